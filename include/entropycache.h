@@ -1,0 +1,245 @@
+/*
+ * entropycache.h — C ABI of the EntropyCache denoising-step library (GB300, sm_103a).
+ *
+ * One denoising step of EntropyCache, the training-free KV-cache policy for diffusion
+ * language models described in "EntropyCache: Decoded Token Entropy Guided KV Caching for
+ * Diffusion Language Models" (Cheong, Son, Lim, Yoo; summaries at gist.science, zh and pt):
+ *
+ *   (a) softmax + greedy decode + Shannon entropy over the V-wide logits of each masked
+ *       candidate position                         -> ec_entropy_decode
+ *   (b) commit the decoded tokens, take the maximum entropy E of the newly decoded tokens
+ *       and compare it with tau (full recompute iff E > tau)
+ *   (c) push the new tokens onto the decode history and build the recompute set
+ *       (still-masked positions plus the last k decoded ones; every position on a full
+ *       step)                                      -> ec_select_recompute (b + c)
+ *       then write the fresh K/V rows of that set into the layer's cache
+ *                                                  -> ec_kv_scatter
+ *   (d) bidirectional attention of the recompute rows against all L cached rows
+ *                                                  -> ec_partial_attention
+ *   ec_step runs (a)(b)(c) once and then (c-scatter)(d) for every layer.
+ *
+ * Conventions shared by every entry point
+ *   - Every call returns an ec_status and never throws or aborts.
+ *   - Every data pointer is a DEVICE pointer owned by the caller (allocated by any means,
+ *     e.g. PyTorch). The library allocates and frees no memory: scratch space is a
+ *     caller-provided workspace whose size the matching *_workspace_size() call returns.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL = legacy default
+ *     stream). Outputs are valid once the stream has synchronised.
+ *   - Arguments are validated on the host before any launch. On a validation error
+ *     nothing is launched and EC_ERR_INVALID_ARG / EC_ERR_UNSUPPORTED is returned.
+ *   - Data the host cannot see (positions, indices) is checked on the device. A bad
+ *     element is skipped and a bit is OR-ed into the caller's device error word
+ *     (`dev_err`, one int32, may be NULL); ec_read_device_error() reports it.
+ *   - Shapes are in elements, tensors are dense row-major in the order written, and every
+ *     base pointer must be 16-byte aligned.
+ *   - bf16 means IEEE-754 binary32 truncated to its upper 16 bits (round-to-nearest-even
+ *     when produced); fp32 is IEEE binary32. Entropies are in nats (natural logarithm).
+ */
+#ifndef ENTROPYCACHE_H_
+#define ENTROPYCACHE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------------------- */
+typedef int32_t ec_status;
+#define EC_OK 0
+#define EC_ERR_INVALID_ARG 1   /* a null pointer, a bad size, a misaligned pointer       */
+#define EC_ERR_UNSUPPORTED 2   /* a valid request this build does not implement          */
+#define EC_ERR_CUDA 3          /* a CUDA runtime/driver call failed                      */
+#define EC_ERR_DEVICE_CHECK 4  /* a device-side bounds/consistency check fired           */
+#define EC_ERR_TIMEOUT 5       /* a bounded device-side wait gave up                     */
+
+/* Bits of the device error word. */
+#define EC_DEVERR_BAD_CAND_POS 0x1  /* candidate position outside [0, L) or not masked   */
+#define EC_DEVERR_BAD_IDX 0x2       /* recompute index outside [0, L)                    */
+#define EC_DEVERR_BAD_R 0x4         /* recompute-set size outside [0, L]                 */
+#define EC_DEVERR_TIMEOUT 0x8       /* a bounded pipeline wait ran out                   */
+
+/* ---- logits element types ------------------------------------------------------------ */
+#define EC_F32 0
+#define EC_BF16 1
+
+typedef void* ec_stream_t; /* a cudaStream_t */
+
+/* ---- step parameters ------------------------------------------------------------------
+ * B      sequences in the batch (1 <= B <= 4096)
+ * L      positions per sequence, prompt + generation (1 <= L <= 1048576)
+ * Hq     query heads; Hkv key/value heads; Hq % Hkv == 0 and Hq / Hkv <= 128
+ *        (grouped-query attention: query head h reads key/value head h / (Hq / Hkv))
+ * D      head dimension, 64 or 128
+ * V      vocabulary size (1 <= V <= 2^30)
+ * C_max  candidate rows per sequence: the masked positions of the current block whose
+ *        logits the step receives (1 <= C_max <= min(L, 1024))
+ * k      decode-history length: how many of the most recently decoded positions a
+ *        partial step recomputes (1 <= k <= L)
+ * n_dec  tokens committed per sequence per step (1 <= n_dec <= C_max)
+ * tau    entropy threshold in nats: a step whose decoded tokens' maximum entropy is
+ *        strictly above tau triggers a full recompute
+ * logits_dtype  EC_F32 or EC_BF16
+ */
+typedef struct ec_params {
+  int32_t B, L, Hq, Hkv, D, V, C_max, k, n_dec;
+  float tau;
+  int32_t logits_dtype;
+} ec_params;
+
+/* ---- per-sequence decode state (all device arrays, caller-owned) ----------------------
+ * tokens     int32 [B, L]   committed token id per position (untouched where masked)
+ * mask       uint8 [B, L]   1 = position still masked, 0 = decoded
+ * ring       int32 [B, k]   decode history: ring[b, (head - 1 - t) mod k] is the t-th
+ *                           most recently decoded position, for t < count
+ * ring_head  int32 [B]      next ring slot to write
+ * ring_count int32 [B]      entries held, saturating at k
+ * dec_pos    int32 [B, n_dec]  positions committed by the last step, ascending, -1 padded
+ * E          fp32  [B]      max entropy over the tokens committed by the last step
+ * flag       uint8 [B]      1 = full recompute (E > tau or E is NaN), 0 = partial
+ * idx        int32 [B, L]   recompute set in ascending position order; first R[b] valid
+ * R          int32 [B]      recompute-set size
+ * dev_err    int32 [1]      device error word (EC_DEVERR_* bits OR-ed in), may be NULL
+ */
+typedef struct ec_state {
+  int32_t* tokens;
+  uint8_t* mask;
+  int32_t* ring;
+  int32_t* ring_head;
+  int32_t* ring_count;
+  int32_t* dec_pos;
+  float* E;
+  uint8_t* flag;
+  int32_t* idx;
+  int32_t* R;
+  int32_t* dev_err;
+} ec_state;
+
+/* ---- error reporting ------------------------------------------------------------------ */
+
+/* Human-readable name of a status code; never NULL. */
+const char* ec_status_string(ec_status st);
+
+/* Synchronises `stream`, copies the device error word to *host_word (if non-NULL) and
+ * returns EC_OK when it is zero, EC_ERR_TIMEOUT when the EC_DEVERR_TIMEOUT bit is set,
+ * else EC_ERR_DEVICE_CHECK. Does not clear the word. */
+ec_status ec_read_device_error(const int32_t* dev_err, int32_t* host_word, ec_stream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t ec_version(void);
+
+/* ---- (a) fused softmax / argmax decode / entropy ---------------------------------------
+ * Follows the decode-and-entropy stage of the EntropyCache workflow (zh summary §2.2: the
+ * new tokens are decoded from the logits and the entropy -sum_j p_ij log p_ij of each is
+ * evaluated; pt summary §2 "Fluxo de Funcionamento"), per row i:
+ *   m_i = max_j x_ij, ids[i] = the LOWEST j with x_ij == m_i (greedy decode),
+ *   p_ij = exp(x_ij - m_i) / sum_j exp(x_ij - m_i)   (softmax at temperature 1),
+ *   entropy[i]  = -sum_j p_ij ln p_ij  (0 ln 0 = 0),
+ *   log_conf[i] = ln p_{i, ids[i]}     (log-probability of the decoded token).
+ * logits     [n_rows, row_stride] of `dtype` (EC_F32 / EC_BF16); the first V entries of
+ *            each row are read. row_stride >= V and row_stride * elem_size % 16 == 0.
+ * ids        int32 [n_rows]; entropy, log_conf fp32 [n_rows].
+ * ws         workspace of at least ec_entropy_decode_workspace_size(n_rows, V, dtype)
+ *            bytes; it must be zero-filled before its first use and the library leaves it
+ *            ready for the next call (its counters return to zero). Calls that share a
+ *            workspace must not overlap in time.
+ * Accumulation is fp32; argmax compares the raw stored values, so ids are exact. -inf
+ * logits contribute zero probability. NaN logits are not supported (results undefined).
+ * n_rows == 0 is a valid no-op. */
+size_t ec_entropy_decode_workspace_size(int32_t n_rows, int32_t V, int32_t dtype);
+ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
+                            int32_t dtype, int32_t* ids, float* entropy, float* log_conf,
+                            void* ws, size_t ws_bytes, ec_stream_t stream);
+
+/* ---- (b)+(c) commit, max-entropy gate, decode history, recompute set -------------------
+ * Follows the skip decision and selection stage of the workflow (zh summary §2.2: full
+ * recompute iff E_{t+1} = max over newly decoded tokens of their entropy exceeds tau,
+ * else reuse the cache except the current masked tokens and the k most recently decoded
+ * tokens, taken from a decode history; §2.3: O(k) memory for the history; pt summary §2
+ * "Decisão de Pulo", "Histórico de Decodificação"). Per sequence b:
+ *   1. D = the n_dec candidates i < cand_count[b] with the largest log_conf (a NaN
+ *      log_conf ranks lowest; ties go to the smaller position cand_pos[b, i]).
+ *   2. tokens[b, cand_pos] = ids, mask[b, cand_pos] = 0 for i in D; dec_pos[b] = the
+ *      positions of D ascending, -1 padded.
+ *   3. E[b] = max over D of entropy (0 when D is empty); flag[b] = E[b] > tau, or 1 when
+ *      E[b] is NaN.
+ *   4. The positions of D are pushed onto the ring in ascending order (count saturates
+ *      at k).
+ *   5. flag = 1: idx[b] = 0..L-1, R[b] = L. flag = 0: idx[b] = the ascending list of
+ *      positions p with mask[b, p] = 1 (after step 2) or p among the last min(k, count)
+ *      ring entries; R[b] = its length.
+ * cand_pos   int32 [B, C_max]; cand_count int32 [B] (0 <= count <= C_max).
+ * ids, entropy, log_conf  as produced by ec_entropy_decode for the B*C_max rows
+ *            (row b*C_max + i belongs to cand_pos[b, i]).
+ * A candidate position outside [0, L) or not masked sets EC_DEVERR_BAD_CAND_POS and is
+ * dropped from the candidate list; a bad cand_count is clamped to [0, C_max] and sets
+ * EC_DEVERR_BAD_R. */
+ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int32_t* cand_pos,
+                              const int32_t* cand_count, const int32_t* ids,
+                              const float* entropy, const float* log_conf, ec_stream_t stream);
+
+/* ---- (c) K/V cache refresh ---------------------------------------------------------------
+ * Recomputed positions receive fresh K/V, all other positions keep their cached rows
+ * (zh summary §2.2, partial forward: only the recompute set is recomputed, the rest is
+ * read from the cache; a full forward refreshes every row). For r < R[b]:
+ *   k_cache[b, idx[b, r], :, :] = k_new[b, src_row, :, :]   (same for v)
+ * where src_row = r when src_by_position == 0 (k_new holds the fresh rows in recompute
+ * order) and src_row = idx[b, r] when src_by_position == 1 (k_new is indexed by position).
+ * k_cache, v_cache  bf16 [B, L, Hkv, D]; k_new, v_new bf16 [B, L, Hkv, D].
+ * idx int32 [B, L], R int32 [B] on the device. An idx outside [0, L) sets
+ * EC_DEVERR_BAD_IDX and that row is skipped; R outside [0, L] sets EC_DEVERR_BAD_R and
+ * that sequence is skipped. k_new/v_new must not overlap the caches. */
+ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const void* k_new,
+                        const void* v_new, int32_t src_by_position, const int32_t* idx,
+                        const int32_t* R, int32_t* dev_err, ec_stream_t stream);
+
+/* ---- (d) partial (or full) bidirectional attention ---------------------------------------
+ * Attention of the recompute rows against every cached row, with no causal mask (dLLMs
+ * attend bidirectionally: zh summary §1; pt summary §1 "Atenção Bidirecional"). For
+ * b < B, r < R[b], query head h (g = Hq / Hkv, kv head = h / g):
+ *   s_j = scale * <q[b, r, h, :], k_cache[b, j, h/g, :]>   for j < L
+ *   out[b, r, h, :] = sum_j softmax(s)_j * v_cache[b, j, h/g, :]
+ * With R[b] = L and q in position order this is dense bidirectional attention (the full
+ * recompute of the pt summary §2 "Decisão de Pulo").
+ * q, out  bf16 [B, L, Hq, D] (rows in recompute order, first R[b] valid; rows >= R[b]
+ *         of out are not written); k_cache, v_cache bf16 [B, L, Hkv, D].
+ * R       int32 [B] on the device (read by the kernel: no host synchronisation).
+ * scale   softmax scale, normally 1/sqrt(D).
+ * ws      at least ec_partial_attention_workspace_size(p) bytes, zero-filled before its
+ *         first use; the library returns its counters to zero. Calls sharing a workspace
+ *         must not overlap in time.
+ * Products run on bf16 tensor cores with fp32 accumulation; probabilities are rounded to
+ * bf16 before the PV product. A pipeline wait that exceeds its limit sets
+ * EC_DEVERR_TIMEOUT in dev_err (if given) and leaves that tile unwritten. */
+size_t ec_partial_attention_workspace_size(const ec_params* p);
+ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* R, float scale, void* out,
+                               void* ws, size_t ws_bytes, int32_t* dev_err, ec_stream_t stream);
+
+/* ---- one whole denoising step ---------------------------------------------------------------
+ * Runs the three stages of the workflow in order (zh summary §2.2): (a) decode and
+ * entropy over the B*C_max candidate rows of `logits` ([B, C_max, V], row stride V);
+ * (b)+(c) the gate and recompute set, updating `st`; then, for each of n_layers layers,
+ * the K/V refresh of the recompute set from the position-indexed fresh rows k_src[l],
+ * v_src[l] (bf16 [B, L, Hkv, D]) into k_cache[l], v_cache[l], the gather of the recompute
+ * rows' queries from q_src[l] (bf16 [B, L, Hq, D], position-indexed) and the attention of
+ * those rows against the refreshed cache into out[l] (bf16 [B, L, Hq, D], recompute
+ * order). One flag and one recompute set serve every layer (zh summary §2.3: the decision
+ * is independent of depth). The flag computed from this step's logits governs this
+ * call's attention stage, which stands for the next forward pass of the workflow.
+ * The pointer arrays k_cache ... out are HOST arrays of n_layers device pointers.
+ * cand_pos, cand_count: as for ec_select_recompute.
+ * ws at least ec_step_workspace_size(p) bytes, zero-filled before its first use.
+ * scale as for ec_partial_attention. */
+size_t ec_step_workspace_size(const ec_params* p);
+ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits,
+                  const int32_t* cand_pos, const int32_t* cand_count, int32_t n_layers,
+                  void* const* k_cache, void* const* v_cache, const void* const* k_src,
+                  const void* const* v_src, const void* const* q_src, void* const* out,
+                  float scale, void* ws, size_t ws_bytes, ec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ENTROPYCACHE_H_ */

@@ -1,0 +1,288 @@
+"""Float64 CPU oracle for one EntropyCache denoising step.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, plain reference that the CUDA library
+is checked against. Only the test suite, the smoke check and the CPU-baseline leg of the
+benchmark may import it; the product path (the C-ABI library and its Python binding) never
+does, and there is no fallback from the product path to this code.
+
+It shares no code with the CUDA path: no kernels, headers, helpers or tables. Inputs arrive
+as NumPy arrays in their stored form (bf16 as uint16 bit patterns, fp32, int32) and are
+widened exactly to float64 here.
+
+Source of the method: "EntropyCache: Decoded Token Entropy Guided KV Caching for Diffusion
+Language Models" (Cheong, Son, Lim, Yoo), in the two gist.science summaries of it:
+  [zh] gist.science/zh/paper/2603.18489, §2.2 "EntropyCache Workflow" (the three stages of
+       a denoising step and the max-entropy equation), §2.3 (O(V) compute, O(k) memory);
+  [pt] gist.science/pt/paper/2603.18489, §1 "O Problema" (bidirectional attention), §2
+       "Metodologia" / "Fluxo de Funcionamento" (decode, skip-or-recompute, history).
+
+Readings where the pages are silent (each also listed in the design notes):
+  - entropy uses the natural logarithm; softmax temperature is 1;
+  - "decode" is greedy argmax, ties to the lowest vocabulary index;
+  - the tokens decoded in a step (the set D) are the n_dec candidates with the highest
+    confidence p(argmax), ties to the lower position; a NaN confidence ranks lowest;
+  - an empty D gives E = 0 (partial); a NaN E gives a full step; E == tau is partial;
+  - the history pushes D in ascending position order and survives full steps;
+  - attention is unmasked (bidirectional) with scale 1/sqrt(D) by default, query head h
+    reading key/value head h // (Hq // Hkv).
+
+Every function here is pinned by tests that do not re-derive it (closed forms, invariants,
+brute force over tiny inputs, and a library attention routine); see tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "widen",
+    "entropy_decode_row",
+    "entropy_decode",
+    "select_decoded",
+    "max_entropy",
+    "recompute_flag",
+    "history_push",
+    "history_last",
+    "recompute_set",
+    "kv_scatter",
+    "attention",
+    "step",
+]
+
+
+# --------------------------------------------------------------------------------------
+# stored dtypes -> float64
+
+
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 value of stored elements: dtype 'bf16' (uint16 bit patterns) or 'f32'."""
+    if dtype == "bf16":
+        bits = np.asarray(a, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+        return bits.view(np.float32).astype(np.float64)
+    if dtype == "f32":
+        return np.asarray(a, dtype=np.float32).astype(np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+# --------------------------------------------------------------------------------------
+# (a) decode + entropy  —  [zh] §2.2, decode new tokens and E = max_i (-sum_j p_ij log p_ij)
+
+
+def entropy_decode_row(x: np.ndarray) -> tuple[int, float, float]:
+    """Greedy decode, Shannon entropy and log-confidence of one row of logits.
+
+    Follows the definition directly ([zh] §2.2, the bracketed term of the max-entropy
+    equation): p = softmax(x), H = -sum_j p_j ln p_j with 0 ln 0 = 0, the decoded token is
+    the lowest index attaining max x, and log_conf = ln p of that token.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m = x.max()
+    ident = int(np.flatnonzero(x == m)[0])  # lowest index attaining the maximum
+    e = np.exp(x - m)  # exp(-inf) = 0
+    p = e / e.sum()
+    nz = p > 0.0
+    h = float(-np.sum(p[nz] * np.log(p[nz])))
+    log_conf = float(np.log(p[ident]))
+    return ident, h, log_conf
+
+
+def entropy_decode(logits: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Row-wise entropy_decode_row over a [n_rows, V] float64 array."""
+    logits = np.asarray(logits, dtype=np.float64)
+    n = logits.shape[0]
+    ids = np.zeros(n, dtype=np.int64)
+    ent = np.zeros(n, dtype=np.float64)
+    conf = np.zeros(n, dtype=np.float64)
+    for i in range(n):
+        ids[i], ent[i], conf[i] = entropy_decode_row(logits[i])
+    return ids, ent, conf
+
+
+# --------------------------------------------------------------------------------------
+# (b) the decoded set and the max-entropy gate  —  [zh] §2.2, [pt] §2 "Decisão de Pulo"
+
+
+def select_decoded(cand_pos: np.ndarray, count: int, log_conf: np.ndarray, n_dec: int) -> list[int]:
+    """Candidate rows committed this step: the n_dec most confident among the first `count`.
+
+    Ranking key: higher log_conf first (NaN ranks lowest), then the smaller position.
+    Returns candidate row numbers sorted by ascending position.
+    """
+
+    def key(i: int) -> tuple[float, int]:
+        c = float(log_conf[i])
+        if math.isnan(c):
+            c = -math.inf
+        return (-c, int(cand_pos[i]))
+
+    order = sorted(range(int(count)), key=key)
+    chosen = order[: int(n_dec)]
+    return sorted(chosen, key=lambda i: int(cand_pos[i]))
+
+
+def max_entropy(entropy: np.ndarray, decoded_rows: list[int]) -> float:
+    """E_{t+1} = max over the newly decoded tokens of their entropy ([zh] §2.2).
+
+    0 for an empty set; NaN if any entropy in the set is NaN.
+    """
+    if not decoded_rows:
+        return 0.0
+    vals = [float(entropy[i]) for i in decoded_rows]
+    if any(math.isnan(v) for v in vals):
+        return math.nan
+    return max(vals)
+
+
+def recompute_flag(E: float, tau: float) -> bool:
+    """Full recompute iff E > tau ([zh] §2.2; [pt] §2): E == tau reuses the cache; NaN is full."""
+    E = float(E)
+    if math.isnan(E):
+        return True
+    return bool(E > float(tau))
+
+
+# --------------------------------------------------------------------------------------
+# (c) decode history and recompute set  —  [zh] §2.2 / §2.3, [pt] §2 "Histórico"
+
+
+def history_push(ring: np.ndarray, head: int, count: int, positions: list[int]) -> tuple[np.ndarray, int, int]:
+    """Append positions (in the given order) to a FIFO of capacity k = len(ring).
+
+    Slot `head` receives the next entry; the count saturates at k ([zh] §2.3: O(k) memory).
+    """
+    ring = np.array(ring, dtype=np.int64, copy=True)
+    k = ring.shape[0]
+    for p in positions:
+        ring[head] = p
+        head = (head + 1) % k
+        count = min(count + 1, k)
+    return ring, head, count
+
+
+def history_last(ring: np.ndarray, head: int, count: int) -> list[int]:
+    """The last min(k, count) pushed positions, most recent first."""
+    k = len(ring)
+    n = min(int(count), k)
+    return [int(ring[(head - 1 - t) % k]) for t in range(n)]
+
+
+def recompute_set(mask: np.ndarray, recent: list[int], full: bool) -> np.ndarray:
+    """Recompute set of one sequence, ascending ([zh] §2.2 partial forward; [pt] §2).
+
+    Full step: every position. Partial step: still-masked positions union the k most recently
+    decoded positions.
+    """
+    L = mask.shape[0]
+    if full:
+        return np.arange(L, dtype=np.int64)
+    chosen = set(int(p) for p in np.flatnonzero(mask))
+    chosen.update(int(p) for p in recent)
+    return np.array(sorted(chosen), dtype=np.int64)
+
+
+def kv_scatter(cache: np.ndarray, idx: np.ndarray, fresh_rows: np.ndarray) -> np.ndarray:
+    """Cache after refreshing the recompute rows: cache[idx[r]] = fresh_rows[r]."""
+    out = np.array(cache, copy=True)
+    for r, pos in enumerate(idx):
+        out[int(pos)] = fresh_rows[r]
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# (d) bidirectional attention  —  [pt] §1 "Atenção Bidirecional"; [zh] §1
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Unmasked softmax attention of query rows against every key row, in float64.
+
+    q [R, Hq, D], k and v [L, Hkv, D]; query head h reads key/value head h // (Hq // Hkv).
+    out[r, h] = sum_j softmax_j(scale * q[r, h] . k[j, h//g]) v[j, h//g], two-pass softmax
+    (row max subtracted, exponentials, normalisation).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    R, Hq, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    out = np.zeros((R, Hq, D), dtype=np.float64)
+    for h in range(Hq):
+        kv = h // g
+        s = (q[:, h, :] @ k[:, kv, :].T) * scale  # [R, L]
+        s = s - s.max(axis=1, keepdims=True)
+        w = np.exp(s)
+        w = w / w.sum(axis=1, keepdims=True)
+        out[:, h, :] = w @ v[:, kv, :]
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# one whole step  —  [zh] §2.2, the three stages in order
+
+
+def step(
+    *,
+    logits: np.ndarray,
+    cand_pos: np.ndarray,
+    cand_count: int,
+    tokens: np.ndarray,
+    mask: np.ndarray,
+    ring: np.ndarray,
+    ring_head: int,
+    ring_count: int,
+    n_dec: int,
+    tau: float,
+    layers: list[dict] | None = None,
+    scale: float | None = None,
+    attention_rows: np.ndarray | None = None,
+) -> dict:
+    """One denoising step of one sequence.
+
+    logits [C_max, V] float64 (candidate rows); tokens [L]; mask [L] (1 = masked);
+    ring [k] with head/count. Each element of `layers` is a dict of float64 arrays
+    k_cache, v_cache [L, Hkv, D], k_src, v_src [L, Hkv, D] (fresh rows by position) and
+    q_src [L, Hq, D] (queries by position). attention_rows optionally restricts which
+    recompute rows get an attention output (a sample); None computes all of them.
+    Returns decode results, the gate, the new state, idx and per-layer outputs.
+    """
+    C = int(cand_count)
+    ids, ent, conf = entropy_decode(logits[:C]) if C > 0 else (
+        np.zeros(0, np.int64), np.zeros(0), np.zeros(0))
+    rows = select_decoded(cand_pos, C, conf, n_dec)
+    tokens = np.array(tokens, dtype=np.int64, copy=True)
+    mask = np.array(mask, dtype=np.uint8, copy=True)
+    for i in rows:
+        tokens[int(cand_pos[i])] = ids[i]
+        mask[int(cand_pos[i])] = 0
+    E = max_entropy(ent, rows)
+    full = recompute_flag(E, tau)
+    dec_positions = [int(cand_pos[i]) for i in rows]
+    ring2, head2, count2 = history_push(ring, ring_head, ring_count, dec_positions)
+    idx = recompute_set(mask, history_last(ring2, head2, count2), full)
+    out_layers = []
+    for lay in layers or []:
+        kc = kv_scatter(lay["k_cache"], idx, lay["k_src"][idx])
+        vc = kv_scatter(lay["v_cache"], idx, lay["v_src"][idx])
+        D = kc.shape[-1]
+        sc = (1.0 / math.sqrt(D)) if scale is None else scale
+        sel = idx if attention_rows is None else idx[attention_rows]
+        o = attention(lay["q_src"][sel], kc, vc, sc)
+        out_layers.append({"k_cache": kc, "v_cache": vc, "out": o})
+    return {
+        "ids": ids,
+        "entropy": ent,
+        "log_conf": conf,
+        "decoded_rows": rows,
+        "dec_pos": dec_positions,
+        "E": E,
+        "flag": bool(full),
+        "tokens": tokens,
+        "mask": mask,
+        "ring": ring2,
+        "ring_head": head2,
+        "ring_count": count2,
+        "idx": idx,
+        "R": int(idx.shape[0]),
+        "layers": out_layers,
+    }

@@ -1,0 +1,345 @@
+"""Pins of the float64 oracle to facts that do not come from the oracle itself.
+
+Each test checks the oracle against a closed form, an invariant, a library routine computing
+the same quantity, or brute force over tiny inputs, chosen so that a plausible slip (a wrong
+log base, a dropped minus sign, a missing normalisation, a wrong tie rule, a transposed
+operand, an off-by-one in the history) fails at least one of them.
+
+Facts used (EntropyCache, gist.science zh summary §2.2 and pt summary §2):
+  - E_{t+1} = max over the newly decoded tokens of -sum_j p_ij log p_ij;
+  - E > tau triggers a full recompute, E <= tau reuses the cache except masked + last k;
+  - with every position recomputed the attention is plain dense bidirectional attention.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+import oracle as O
+import workloads as W
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# --------------------------------------------------------------------------------------
+# entropy / decode
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 32000, 126464, 152064])
+@pytest.mark.parametrize("c", [0.0, -3.5, 17.25])
+def test_uniform_logits_give_ln_V(V, c):
+    ident, h, lc = O.entropy_decode_row(np.full(V, c))
+    assert abs(h - math.log(V)) <= 1e-12 * max(1.0, math.log(V)) + 1e-12
+    assert abs(lc + math.log(V)) <= 1e-12 * max(1.0, math.log(V)) + 1e-12
+    assert ident == 0  # a V-way tie decodes to the lowest index
+
+
+@pytest.mark.parametrize("hot", [0, 5, 99])
+def test_one_hot_gives_zero(hot):
+    x = np.full(100, -np.inf)
+    x[hot] = 3.0
+    ident, h, lc = O.entropy_decode_row(x)
+    assert ident == hot and h == 0.0 and lc == 0.0
+    y = np.zeros(100)
+    y[hot] = 1e4  # the others underflow to zero probability
+    ident, h, lc = O.entropy_decode_row(y)
+    assert ident == hot and abs(h) < 1e-300 and abs(lc) < 1e-300
+
+
+@pytest.mark.parametrize("kk", [2, 3, 8, 64])
+def test_k_way_tie_gives_ln_k_and_lowest_index(kk):
+    rng = np.random.default_rng(kk)
+    x = np.full(500, -np.inf)
+    pos = np.sort(rng.choice(500, size=kk, replace=False))
+    x[pos] = 1.5
+    ident, h, lc = O.entropy_decode_row(x)
+    assert ident == pos[0]
+    assert abs(h - math.log(kk)) < 1e-13
+    assert abs(lc + math.log(kk)) < 1e-13
+
+
+@pytest.mark.parametrize("a,b", [(0.0, 0.0), (1.0, 0.0), (0.0, 2.5), (-3.0, 4.0), (10.0, -10.0)])
+def test_two_logits_give_binary_entropy(a, b):
+    # softmax of two logits is the logistic sigma(a - b); its entropy is the binary entropy
+    p = 1.0 / (1.0 + math.exp(-(a - b)))
+    hb = -sum(t * math.log(t) for t in (p, 1 - p) if t > 0)
+    ident, h, lc = O.entropy_decode_row(np.array([a, b]))
+    assert abs(h - hb) < 1e-12
+    assert ident == (0 if a >= b else 1)
+    assert abs(lc - math.log(max(p, 1 - p))) < 1e-12
+
+
+def test_matches_scipy_entropy_of_softmax():
+    rng = np.random.default_rng(7)
+    for s in (0.1, 1.0, 4.0, 12.0):
+        x = rng.standard_normal(3001) * s
+        ident, h, lc = O.entropy_decode_row(x)
+        p = scipy.special.softmax(x)
+        assert abs(h - scipy.stats.entropy(p)) < 1e-10
+        assert ident == int(np.argmax(x))
+        assert abs(lc - math.log(p.max())) < 1e-10
+
+
+def test_shift_and_permutation_invariance():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(777) * 3
+    ident, h, lc = O.entropy_decode_row(x)
+    i2, h2, lc2 = O.entropy_decode_row(x + 123.456)
+    assert i2 == ident and abs(h2 - h) < 1e-11 and abs(lc2 - lc) < 1e-11
+    perm = rng.permutation(777)
+    i3, h3, lc3 = O.entropy_decode_row(x[perm])
+    assert perm[i3] == ident and abs(h3 - h) < 1e-11 and abs(lc3 - lc) < 1e-11
+
+
+def test_entropy_bounds_and_neg_inf_entries():
+    rng = np.random.default_rng(3)
+    for V in (2, 10, 1000):
+        x = rng.standard_normal(V) * 5
+        _, h, lc = O.entropy_decode_row(x)
+        assert -1e-12 <= h <= math.log(V) + 1e-12
+        assert lc <= 0
+        # -inf entries carry zero probability and do not change the entropy of the rest
+        y = np.concatenate([x, np.full(13, -np.inf)])
+        _, h2, lc2 = O.entropy_decode_row(y)
+        assert abs(h2 - h) < 1e-12 and abs(lc2 - lc) < 1e-12
+
+
+def test_widen_is_exact():
+    vals = np.array([0.0, 1.0, -2.5, 3.140625, 1e-20, -65280.0], dtype=np.float32)
+    bits = W.to_bf16_bits(vals)
+    back = O.widen(bits, "bf16")
+    assert back.dtype == np.float64
+    np.testing.assert_array_equal(back, np.array([0.0, 1.0, -2.5, 3.140625, back[4], -65280.0]))
+    assert abs(back[4] - 1e-20) / 1e-20 < 2 ** -8
+    np.testing.assert_array_equal(O.widen(vals, "f32"), vals.astype(np.float64))
+
+
+# --------------------------------------------------------------------------------------
+# decoded set, max-entropy gate
+
+
+def _brute_decoded(cand_pos, count, conf, n_dec):
+    """The unique subset S of size min(n_dec, count) whose members all outrank every
+    non-member (higher confidence; equal confidence: smaller position; NaN lowest)."""
+    def better(i, j):
+        ci = -math.inf if math.isnan(conf[i]) else conf[i]
+        cj = -math.inf if math.isnan(conf[j]) else conf[j]
+        return ci > cj or (ci == cj and cand_pos[i] < cand_pos[j])
+
+    n = min(n_dec, count)
+    found = []
+    for S in itertools.combinations(range(count), n):
+        rest = [j for j in range(count) if j not in S]
+        if all(better(i, j) for i in S for j in rest):
+            found.append(sorted(S, key=lambda i: cand_pos[i]))
+    assert len(found) == 1
+    return found[0]
+
+
+def test_select_decoded_brute_force():
+    rng = np.random.default_rng(5)
+    for trial in range(400):
+        C = int(rng.integers(1, 8))
+        count = int(rng.integers(0, C + 1))
+        n_dec = int(rng.integers(1, C + 1))
+        cand_pos = rng.choice(40, size=C, replace=False)
+        conf = -rng.integers(0, 3, size=C).astype(np.float64)  # many exact ties
+        if trial % 7 == 0 and C > 1:
+            conf[rng.integers(0, C)] = np.nan
+        got = O.select_decoded(cand_pos, count, conf, n_dec)
+        assert got == _brute_decoded(cand_pos, count, conf, n_dec)
+
+
+def test_max_entropy_and_flag_boundaries():
+    ent = np.array([0.3, 1.0, 2.5, np.nan])
+    assert O.max_entropy(ent, []) == 0.0
+    assert O.max_entropy(ent, [0, 1]) == 1.0
+    assert O.max_entropy(ent, [0, 2, 1]) == 2.5
+    assert math.isnan(O.max_entropy(ent, [0, 3]))
+    tau = 1.0
+    assert O.recompute_flag(1.0, tau) is False  # E == tau reuses the cache
+    assert O.recompute_flag(np.nextafter(1.0, 2.0), tau) is True
+    assert O.recompute_flag(np.nextafter(1.0, 0.0), tau) is False
+    assert O.recompute_flag(math.nan, tau) is True
+    assert O.recompute_flag(0.0, tau) is False
+
+
+# --------------------------------------------------------------------------------------
+# history and recompute set
+
+
+def test_history_matches_unbounded_list():
+    rng = np.random.default_rng(9)
+    for k in (1, 2, 5, 16):
+        ring = np.zeros(k, dtype=np.int64)
+        head = count = 0
+        full: list[int] = []
+        for _ in range(60):
+            push = [int(v) for v in rng.integers(0, 1000, size=int(rng.integers(0, 4)))]
+            ring, head, count = O.history_push(ring, head, count, push)
+            full.extend(push)
+            assert count == min(len(full), k)
+            assert O.history_last(ring, head, count) == list(reversed(full))[:k]
+
+
+def test_recompute_set_exhaustive_small():
+    rng = np.random.default_rng(13)
+    for L in range(1, 11):
+        for bits in range(1 << L):
+            mask = np.array([(bits >> p) & 1 for p in range(L)], dtype=np.uint8)
+            recent = [int(v) for v in rng.choice(L, size=int(rng.integers(0, L + 1)), replace=False)]
+            got = O.recompute_set(mask, recent, full=False)
+            want = [p for p in range(L) if mask[p] == 1 or p in recent]
+            assert got.tolist() == want
+            assert O.recompute_set(mask, recent, full=True).tolist() == list(range(L))
+
+
+# --------------------------------------------------------------------------------------
+# attention
+
+
+def _sdpa(q, k, v, scale):
+    """torch's scaled_dot_product_attention in float64, GQA by repeating kv heads."""
+    R, Hq, D = q.shape
+    g = Hq // k.shape[1]
+    qt = torch.from_numpy(q).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(k).repeat_interleave(g, dim=1).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v).repeat_interleave(g, dim=1).permute(1, 0, 2)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+@pytest.mark.parametrize("R,L,Hq,Hkv,D", [(5, 17, 2, 2, 8), (16, 16, 4, 1, 16), (3, 40, 6, 2, 64), (1, 1, 1, 1, 4)])
+def test_attention_matches_library_sdpa(R, L, Hq, Hkv, D):
+    rng = np.random.default_rng(R * 1000 + L)
+    q = rng.standard_normal((R, Hq, D))
+    k = rng.standard_normal((L, Hkv, D))
+    v = rng.standard_normal((L, Hkv, D))
+    scale = 1.0 / math.sqrt(D)
+    np.testing.assert_allclose(O.attention(q, k, v, scale), _sdpa(q, k, v, scale), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(21)
+    L, D = 9, 5
+    v = rng.standard_normal((L, 1, D))
+    q = rng.standard_normal((3, 1, D))
+    # all keys equal: uniform weights, output is the mean of the value rows
+    k = np.tile(rng.standard_normal((1, 1, D)), (L, 1, 1))
+    np.testing.assert_allclose(O.attention(q, k, v, 0.7), np.broadcast_to(v.mean(axis=0), (3, 1, D)), atol=1e-13)
+    # one key with a +50 score gap: output is that key's value row
+    k = np.zeros((L, 1, D))
+    k[4, 0, 0] = 50.0
+    qq = np.zeros((1, 1, D))
+    qq[0, 0, 0] = 1.0
+    np.testing.assert_allclose(O.attention(qq, k, v, 1.0)[0, 0], v[4, 0], atol=1e-18 + 1e-20)
+    # D = 1, L = 2 by hand
+    q1 = np.array([[[2.0]]])
+    k1 = np.array([[[1.0]], [[-0.5]]])
+    v1 = np.array([[[3.0]], [[7.0]]])
+    s0, s1 = 2.0 * 1.0 * 0.5, 2.0 * -0.5 * 0.5
+    want = (math.exp(s0) * 3.0 + math.exp(s1) * 7.0) / (math.exp(s0) + math.exp(s1))
+    assert abs(O.attention(q1, k1, v1, 0.5)[0, 0, 0] - want) < 1e-14
+
+
+def test_attention_key_permutation_invariance():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((4, 2, 8))
+    k = rng.standard_normal((30, 1, 8))
+    v = rng.standard_normal((30, 1, 8))
+    perm = rng.permutation(30)
+    np.testing.assert_allclose(O.attention(q, k, v, 0.35), O.attention(q, k[perm], v[perm], 0.35), atol=1e-13)
+
+
+# --------------------------------------------------------------------------------------
+# whole step, brute force on L <= 16
+
+
+def _brute_step(logits, cand_pos, count, tokens, mask, decoded_history, n_dec, tau, k):
+    """List-based restatement of one step: decode all candidates, commit the n_dec most
+    confident, gate on their maximum entropy, recompute masked + last k decoded."""
+    info = []
+    for i in range(count):
+        x = [float(t) for t in logits[i]]
+        m = max(x)
+        ident = x.index(m)
+        z = sum(math.exp(t - m) for t in x)
+        ps = [math.exp(t - m) / z for t in x]
+        h = -sum(p * math.log(p) for p in ps if p > 0)
+        info.append((math.log(ps[ident]), int(cand_pos[i]), ident, h))
+    ranked = sorted(info, key=lambda t: (-t[0], t[1]))[:n_dec]
+    tokens = list(tokens)
+    mask = list(mask)
+    for _, pos, ident, _ in ranked:
+        tokens[pos] = ident
+        mask[pos] = 0
+    E = max((t[3] for t in ranked), default=0.0)
+    full = E > tau
+    hist = list(decoded_history) + sorted(t[1] for t in ranked)
+    recent = set(hist[-k:]) if k > 0 else set()
+    L = len(mask)
+    idx = list(range(L)) if full else [p for p in range(L) if mask[p] or p in recent]
+    return tokens, mask, E, full, idx, hist
+
+
+def test_step_brute_force_tiny():
+    rng = np.random.default_rng(31)
+    for trial in range(300):
+        L = int(rng.integers(2, 17))
+        k = int(rng.integers(1, L + 1))
+        Vv = int(rng.integers(2, 9))
+        mask = (rng.random(L) < 0.5).astype(np.uint8)
+        masked = np.flatnonzero(mask)
+        if masked.size == 0:
+            mask[0] = 1
+            masked = np.array([0])
+        C = int(masked.size)
+        cand_pos = masked.astype(np.int64)
+        count = int(rng.integers(0, C + 1))
+        n_dec = int(rng.integers(1, C + 1))
+        scale = rng.choice([0.05, 1.0, 6.0])
+        logits = rng.standard_normal((C, Vv)) * scale
+        if trial % 5 == 0:
+            logits = np.round(logits)  # exact ties in the argmax and in the confidence
+        tokens = rng.integers(0, Vv, size=L)
+        decoded = [p for p in range(L) if not mask[p]]
+        rng.shuffle(decoded)
+        ring = np.zeros(k, dtype=np.int64)
+        ring, head, cnt = O.history_push(ring, 0, 0, decoded)
+        tau = float(rng.choice([0.0, 0.3, 1.0, 5.0]))
+        got = O.step(logits=logits, cand_pos=cand_pos, cand_count=count, tokens=tokens, mask=mask,
+                     ring=ring, ring_head=head, ring_count=cnt, n_dec=n_dec, tau=tau)
+        t2, m2, E2, f2, idx2, hist2 = _brute_step(logits, cand_pos, count, tokens, mask, decoded, n_dec, tau, k)
+        assert got["tokens"].tolist() == t2
+        assert got["mask"].tolist() == m2
+        assert abs(got["E"] - E2) < 1e-12
+        assert got["flag"] == f2
+        assert got["idx"].tolist() == idx2
+        assert got["R"] == len(idx2)
+        assert O.history_last(got["ring"], got["ring_head"], got["ring_count"]) == list(reversed(hist2))[:k]
+
+
+def test_step_full_flag_attention_is_dense_attention():
+    rng = np.random.default_rng(41)
+    L, Hq, Hkv, D, Vv = 12, 4, 2, 8, 50
+    mask = np.zeros(L, dtype=np.uint8)
+    mask[8:] = 1
+    logits = rng.standard_normal((4, Vv)) * 0.1  # near-uniform: high entropy, full step
+    lay = {
+        "k_cache": rng.standard_normal((L, Hkv, D)),
+        "v_cache": rng.standard_normal((L, Hkv, D)),
+        "k_src": rng.standard_normal((L, Hkv, D)),
+        "v_src": rng.standard_normal((L, Hkv, D)),
+        "q_src": rng.standard_normal((L, Hq, D)),
+    }
+    got = O.step(logits=logits, cand_pos=np.arange(8, 12), cand_count=4, tokens=np.zeros(L, np.int64),
+                 mask=mask, ring=np.zeros(4, np.int64), ring_head=0, ring_count=0, n_dec=1, tau=1.0,
+                 layers=[lay])
+    assert got["flag"] and got["R"] == L
+    out = got["layers"][0]["out"]
+    dense = _sdpa(lay["q_src"], lay["k_src"], lay["v_src"], 1.0 / math.sqrt(D))
+    np.testing.assert_allclose(out, dense, rtol=1e-12, atol=1e-12)

@@ -1,0 +1,223 @@
+"""EntropyCache denoising step on GB300: Python binding of the C ABI (include/entropycache.h).
+
+Argument marshalling only: every stage of the step runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams. The library must be built in-tree first
+(`python -m entropy_gated_kv_gb300.build`); importing the binding does not build it and
+nothing here falls back to a CPU implementation.
+
+Stages (EntropyCache, gist.science zh summary §2.2):
+  entropy_decode     (a) softmax + greedy decode + Shannon entropy per candidate row
+  select_recompute   (b)+(c) commit, max-entropy gate vs tau, decode history, recompute set
+  kv_scatter         (c) fresh K/V rows of the recompute set into the cache
+  partial_attention  (d) bidirectional attention of the recompute rows over all L rows
+  step               all of the above for one denoising step over n layers
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from . import _capi as C
+from ._capi import EcError  # noqa: F401
+
+__all__ = [
+    "Params",
+    "DecodeState",
+    "lib",
+    "workspace",
+    "entropy_decode",
+    "entropy_decode_workspace_size",
+    "select_recompute",
+    "kv_scatter",
+    "partial_attention",
+    "partial_attention_workspace_size",
+    "step",
+    "step_workspace_size",
+    "read_device_error",
+    "EcError",
+]
+
+
+def lib() -> ctypes.CDLL:
+    return C.load()
+
+
+def _vp(t: torch.Tensor | None) -> ctypes.c_void_p | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("EntropyCache kernels take CUDA tensors (there is no CPU path)")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: torch.cuda.Stream | None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(d) -> int:
+    if d in ("bf16", torch.bfloat16, C.EC_BF16):
+        return C.EC_BF16
+    if d in ("f32", torch.float32, C.EC_F32):
+        return C.EC_F32
+    raise ValueError(f"unsupported logits dtype {d!r}")
+
+
+@dataclass
+class Params:
+    """Step shape and knobs (ec_params)."""
+
+    B: int
+    L: int
+    Hq: int
+    Hkv: int
+    D: int
+    V: int
+    C_max: int
+    k: int
+    n_dec: int = 1
+    tau: float = 1.0
+    logits_dtype: object = "bf16"
+
+    def c(self) -> C.EcParams:
+        return C.EcParams(self.B, self.L, self.Hq, self.Hkv, self.D, self.V, self.C_max, self.k, self.n_dec,
+                          float(self.tau), _dtype_code(self.logits_dtype))
+
+
+class DecodeState:
+    """Per-sequence decode state (ec_state) as CUDA tensors."""
+
+    FIELDS = ("tokens", "mask", "ring", "ring_head", "ring_count", "dec_pos", "E", "flag", "idx", "R", "dev_err")
+
+    def __init__(self, p: Params, device="cuda"):
+        B, L, k = p.B, p.L, p.k
+        z = lambda *s, dt=torch.int32: torch.zeros(*s, dtype=dt, device=device)  # noqa: E731
+        self.tokens = z(B, L)
+        self.mask = z(B, L, dt=torch.uint8)
+        self.ring = z(B, k)
+        self.ring_head = z(B)
+        self.ring_count = z(B)
+        self.dec_pos = z(B, p.n_dec)
+        self.E = z(B, dt=torch.float32)
+        self.flag = z(B, dt=torch.uint8)
+        self.idx = z(B, L)
+        self.R = z(B)
+        self.dev_err = z(1)
+
+    @classmethod
+    def from_arrays(cls, p: Params, device="cuda", **arrays) -> "DecodeState":
+        st = cls(p, device)
+        for name, a in arrays.items():
+            getattr(st, name).copy_(torch.as_tensor(a).to(getattr(st, name).dtype))
+        return st
+
+    def c(self) -> C.EcState:
+        return C.EcState(*[_vp(getattr(self, f)) for f in self.FIELDS])
+
+    def clone(self) -> "DecodeState":
+        other = object.__new__(DecodeState)
+        for f in self.FIELDS:
+            setattr(other, f, getattr(self, f).clone())
+        return other
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """Zero-filled scratch buffer (the library keeps its counters at zero between calls)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def entropy_decode_workspace_size(n_rows: int, V: int, dtype) -> int:
+    return int(lib().ec_entropy_decode_workspace_size(n_rows, V, _dtype_code(dtype)))
+
+
+def entropy_decode(logits: torch.Tensor, V: int | None = None, ws: torch.Tensor | None = None,
+                   out: tuple | None = None, stream=None):
+    """(a) ids int32, entropy fp32, log_conf fp32 for each row of logits [n_rows, row_stride]."""
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [n_rows, row_stride] with unit inner stride")
+    n, V = logits.shape[0], (V if V is not None else logits.shape[1])
+    code = _dtype_code(logits.dtype)
+    if out is None:
+        out = (torch.empty(n, dtype=torch.int32, device=logits.device),
+               torch.empty(n, dtype=torch.float32, device=logits.device),
+               torch.empty(n, dtype=torch.float32, device=logits.device))
+    if ws is None:
+        ws = workspace(entropy_decode_workspace_size(n, V, code), logits.device)
+    st = lib().ec_entropy_decode(_vp(logits), logits.stride(0), n, V, code, _vp(out[0]), _vp(out[1]), _vp(out[2]),
+                                 _vp(ws), ws.numel(), _stream(stream))
+    C.check(st, "ec_entropy_decode")
+    return out
+
+
+def select_recompute(p: Params, state: DecodeState, cand_pos, cand_count, ids, entropy, log_conf, stream=None):
+    """(b)+(c) commit, gate, history push and recompute set; updates `state` in place."""
+    pc, sc = p.c(), state.c()
+    st = lib().ec_select_recompute(ctypes.byref(pc), ctypes.byref(sc), _vp(cand_pos), _vp(cand_count), _vp(ids),
+                                   _vp(entropy), _vp(log_conf), _stream(stream))
+    C.check(st, "ec_select_recompute")
+
+
+def kv_scatter(p: Params, k_cache, v_cache, k_new, v_new, idx, R, src_by_position: bool = False,
+               dev_err=None, stream=None):
+    """(c) k_cache[b, idx[b, r]] = k_new[b, r or idx[b, r]] (same for v) for r < R[b]."""
+    pc = p.c()
+    st = lib().ec_kv_scatter(ctypes.byref(pc), _vp(k_cache), _vp(v_cache), _vp(k_new), _vp(v_new),
+                             int(bool(src_by_position)), _vp(idx), _vp(R), _vp(dev_err), _stream(stream))
+    C.check(st, "ec_kv_scatter")
+
+
+def partial_attention_workspace_size(p: Params) -> int:
+    pc = p.c()
+    return int(lib().ec_partial_attention_workspace_size(ctypes.byref(pc)))
+
+
+def partial_attention(p: Params, q, k_cache, v_cache, R, out, scale: float | None = None,
+                      ws: torch.Tensor | None = None, dev_err=None, stream=None):
+    """(d) out[b, r, h] = softmax(scale q k^T) v over all L keys, for r < R[b]."""
+    pc = p.c()
+    if ws is None:
+        ws = workspace(partial_attention_workspace_size(p), q.device)
+    sc = (1.0 / math.sqrt(p.D)) if scale is None else float(scale)
+    st = lib().ec_partial_attention(ctypes.byref(pc), _vp(q), _vp(k_cache), _vp(v_cache), _vp(R), sc, _vp(out),
+                                    _vp(ws), ws.numel(), _vp(dev_err), _stream(stream))
+    C.check(st, "ec_partial_attention")
+    return out
+
+
+def step_workspace_size(p: Params) -> int:
+    pc = p.c()
+    return int(lib().ec_step_workspace_size(ctypes.byref(pc)))
+
+
+def _ptr_array(ts) -> ctypes.Array:
+    arr = (ctypes.c_void_p * max(1, len(ts)))()
+    for i, t in enumerate(ts):
+        arr[i] = t.data_ptr()
+    return arr
+
+
+def step(p: Params, state: DecodeState, logits, cand_pos, cand_count, layers: list[dict],
+         scale: float | None = None, ws: torch.Tensor | None = None, stream=None):
+    """One denoising step: (a)(b)(c) once, then scatter + attention for each layer.
+
+    layers: dicts with k_cache, v_cache, k_src, v_src, q_src and out (CUDA bf16 tensors).
+    """
+    pc, sc = p.c(), state.c()
+    if ws is None:
+        ws = workspace(step_workspace_size(p), logits.device)
+    names = ("k_cache", "v_cache", "k_src", "v_src", "q_src", "out")
+    arrs = [_ptr_array([lay[n] for lay in layers]) for n in names]
+    sc_ = (1.0 / math.sqrt(p.D)) if scale is None else float(scale)
+    st = lib().ec_step(ctypes.byref(pc), ctypes.byref(sc), _vp(logits), _vp(cand_pos), _vp(cand_count), len(layers),
+                       *arrs, sc_, _vp(ws), ws.numel(), _stream(stream))
+    C.check(st, "ec_step")
+
+
+def read_device_error(dev_err: torch.Tensor, stream=None) -> tuple[int, int]:
+    """Synchronises the stream and returns (status, device error word)."""
+    w = ctypes.c_int32(0)
+    st = lib().ec_read_device_error(_vp(dev_err), ctypes.byref(w), _stream(stream))
+    return int(st), int(w.value)

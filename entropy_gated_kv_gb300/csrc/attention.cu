@@ -1,0 +1,592 @@
+// attention.cu — stage (d) of the EntropyCache step: bidirectional attention of the
+// recompute rows against every cached K/V row, on the 5th-generation tensor cores.
+//
+// EntropyCache, gist.science pt summary §1 ("Atenção Bidirecional") and zh summary §1: dLLMs
+// attend bidirectionally, so a recomputed row attends to all L positions, none masked; zh
+// §2.2: the partial forward recomputes only the recompute set and reads the rest from the
+// cache; pt §2: a full recompute refreshes every row (R = L: dense attention).
+//   out[b, r, h] = sum_j softmax_j(scale <q[b, r, h], k[b, j, h/g]>) v[b, j, h/g],  r < R[b]
+//
+// Structure (one CTA per SM, persistent, 6 warps):
+//   warp 0      TMA producer: the query tile once per work item, then K and V blocks of
+//               128 keys into a 2-stage ring (128-byte swizzle, mbarrier transaction counts).
+//   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma: S = Q K^T into one
+//               of two TMEM S buffers, and O += P V into the TMEM O accumulator; completion
+//               is signalled with tcgen05.commit on mbarriers.
+//   warps 2..5  softmax and epilogue, one TMEM lane (= one packed query row) per thread:
+//               tcgen05.ld of the S row, online softmax in base 2 with a lazy rescale of O
+//               (only when the running max grows by more than 2^8), P in bf16 written to
+//               shared memory in the swizzled K-major layout the next MMA reads.
+// Grouped-query attention packs the g = Hq / Hkv query heads of one KV head into the 128 MMA
+// rows (floor(128 / g) query rows per tile), so K/V are read once per KV head.
+// Work items (b, kv head, row tile, KV split) are derived on the device from R[], so the
+// kernel needs no host synchronisation. When there are fewer row tiles than CTAs the key
+// range is split; each split writes an unnormalised partial (O, running max, running sum)
+// and the last split to finish (a counter per tile, no spinning) merges them by
+// log-sum-exp weights — the split-KV-then-merge idea of "Prefilling-dLLM" (gist.science pt
+// summary, "Otimização de Kernel de Atenção").
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "ec_common.cuh"
+#include "ec_internal.h"
+
+namespace ec {
+namespace {
+
+constexpr int kBlockM = 128;  // packed query rows per tile (TMEM lanes)
+constexpr int kBlockN = 128;  // keys per KV block
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;    // S buffers at columns [0, 128) and [128, 256)
+constexpr uint32_t kTmemO = 256;  // O accumulator at columns [256, 256 + D)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.f;
+constexpr int kMaxGrid = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], p_free[2];
+  uint64_t pv_done, o_full, o_free;
+  uint32_t tmem_base;
+  int abort;
+  int last_flag;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kAtoms = D / 64;                  // 64 bf16 = 128 bytes per swizzle row
+  static constexpr int kAtomBytes = 128 * 128;           // 128 rows x 128 bytes
+  static constexpr int kQBytes = kAtoms * kAtomBytes;
+  static constexpr int kKVBytes = kAtoms * kAtomBytes;   // one of K or V for one block
+  static constexpr int kStageBytes = 2 * kKVBytes;
+  static constexpr int kPBytes = 2 * kAtomBytes;         // 128 rows x 128 keys
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kQOff + kQBytes;
+  static constexpr int kPOff = kStageOff + 2 * kStageBytes;
+  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kBytes = kBarOff + static_cast<int>(sizeof(Bars));
+  static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct Plan {
+  int tiles;   // row tiles over all (b, kv head)
+  int splits;  // key splits per tile
+  int bps;     // KV blocks per split
+  int nkv;     // KV blocks per sequence
+};
+
+struct Item {
+  int b, kvh, r0, nrows, kb0, nblk, kv_end, tile, split;
+};
+
+__device__ __forceinline__ int clamp_r(int r, int L) { return min(max(r, 0), L); }
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Whole warp; every warp of every CTA computes the same plan.
+__device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int grid) {
+  const int lane = threadIdx.x & 31;
+  int t = 0;
+  for (int b = lane; b < B; b += 32) t += Hkv * ((clamp_r(__ldg(R + b), L) + nr - 1) / nr);
+  t = warp_sum(t);
+  Plan p;
+  p.tiles = t;
+  p.nkv = (L + kBlockN - 1) / kBlockN;
+  int s = 1;
+  if (t > 0 && t < grid) s = min(p.nkv, grid / t);
+  p.bps = (p.nkv + s - 1) / s;
+  p.splits = (p.nkv + p.bps - 1) / p.bps;
+  return p;
+}
+
+// Whole warp. Items are ordered (b, kv head, row tile, split).
+__device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, int L, int Hkv, int nr) {
+  const int lane = threadIdx.x & 31;
+  Item it{};
+  const int tile = item / pl.splits;
+  it.tile = tile;
+  it.split = item - tile * pl.splits;
+  int base = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const int rb = b < B ? clamp_r(__ldg(R + b), L) : 0;
+    const int tb = b < B ? Hkv * ((rb + nr - 1) / nr) : 0;
+    int incl = tb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (tile < base + total) {
+      const unsigned hit = __ballot_sync(0xffffffffu, base + incl > tile);
+      const int src = __ffs(hit) - 1;
+      const int excl = __shfl_sync(0xffffffffu, incl - tb, src);
+      const int rsel = __shfl_sync(0xffffffffu, rb, src);
+      const int mt_count = (rsel + nr - 1) / nr;
+      const int within = tile - base - excl;
+      it.b = b0 + src;
+      it.kvh = within / mt_count;
+      const int mt = within - it.kvh * mt_count;
+      it.r0 = mt * nr;
+      it.nrows = min(nr, rsel - it.r0);
+      break;
+    }
+    base += total;
+  }
+  it.kb0 = it.split * pl.bps;
+  const int kb1 = min(pl.nkv, it.kb0 + pl.bps);
+  it.nblk = kb1 - it.kb0;
+  it.kv_end = min(L, kb1 * kBlockN);
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attention_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Hq, int Hkv, int g,
+    int nr, float scale_log2, uint16_t* __restrict__ out, float* __restrict__ part, uint32_t* __restrict__ counters,
+    int32_t* __restrict__ dev_err) {
+  using LY = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + LY::kBarOff);
+  uint8_t* q_smem = smem + LY::kQOff;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M_rows = nr * g;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 128);
+      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_free[i], 1);
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_free, 128);
+    bars->abort = 0;
+    bars->last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort_flag = &bars->abort;
+
+  const Plan pl = make_plan(R, B, L, Hkv, nr, gridDim.x);
+  const int n_items = pl.tiles * pl.splits;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    uint32_t it = 0;
+    int n = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      int ok = 1;
+      if (lane == 0) {
+        if (n > 0) ok = mbar_wait_bounded(&bars->q_empty, (n - 1) & 1, abort_flag, dev_err, kWaitLimitNs);
+        if (ok) {
+          mbar_arrive_expect_tx(&bars->q_full, LY::kAtoms * M_rows * 128);
+          for (int a = 0; a < LY::kAtoms; ++a)
+            tma_load_5d(q_smem + a * LY::kAtomBytes, &tm_q, &bars->q_full, a * 64, 0, I.kvh, I.r0, I.b);
+        }
+        for (int j = 0; ok && j < I.nblk; ++j) {
+          const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+          ok = mbar_wait_bounded(&bars->kv_empty[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
+          if (!ok) break;
+          uint8_t* kst = smem + LY::kStageOff + slot * LY::kStageBytes;
+          uint8_t* vst = kst + LY::kKVBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[slot], LY::kStageBytes);
+          const int key0 = (I.kb0 + j) * kBlockN;
+          for (int a = 0; a < LY::kAtoms; ++a)
+            tma_load_4d(kst + a * LY::kAtomBytes, &tm_k, &bars->kv_full[slot], a * 64, I.kvh, key0, I.b);
+          for (int a = 0; a < LY::kAtoms; ++a)
+            tma_load_4d(vst + a * LY::kAtomBytes, &tm_v, &bars->kv_full[slot], a * 64, I.kvh, key0, I.b);
+        }
+      }
+      it += I.nblk;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
+    const uint32_t q_addr = smem_u32(q_smem);
+    uint32_t it = 0;
+    int n = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&bars->q_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
+        for (int j = 0; ok && j <= I.nblk; ++j) {
+          if (j < I.nblk) {
+            const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+            ok = mbar_wait_bounded(&bars->kv_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs) &&
+                 mbar_wait_bounded(&bars->s_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(smem + LY::kStageOff + slot * LY::kStageBytes);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * LY::kAtomBytes + (kk & 3) * 32;
+              umma_bf16(tmem + kTmemS + slot * kBlockN, smem_desc_sw128(q_addr + off, 16, 1024),
+                        smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&bars->s_full[slot]);
+            if (j == I.nblk - 1) umma_commit(&bars->q_empty);
+          }
+          if (j >= 1) {
+            const uint32_t prev = it + j - 1, ps = prev & 1u, pu = prev >> 1;
+            if (j == 1 && n > 0)
+              ok = mbar_wait_bounded(&bars->o_free, (n - 1) & 1, abort_flag, dev_err, kWaitLimitNs);
+            ok = ok && mbar_wait_bounded(&bars->p_full[ps], pu & 1u, abort_flag, dev_err, kWaitLimitNs);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t p_addr = smem_u32(smem + LY::kPOff + ps * LY::kPBytes);
+            const uint32_t v_addr = smem_u32(smem + LY::kStageOff + ps * LY::kStageBytes + LY::kKVBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+              const uint32_t a_off = (kk >> 2) * LY::kAtomBytes + (kk & 3) * 32;
+              umma_bf16(tmem + kTmemO, smem_desc_sw128(p_addr + a_off, 16, 1024),
+                        smem_desc_sw128(v_addr + kk * 2048, LY::kAtomBytes, 1024), idesc_pv,
+                        (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(&bars->kv_empty[ps]);
+            umma_commit(&bars->p_free[ps]);
+            umma_commit(&bars->pv_done);
+            if (j == I.nblk) umma_commit(&bars->o_full);
+          }
+        }
+      }
+      it += I.nblk;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int row = 32 * (warp & 3) + lane;  // TMEM lane = packed query row
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint8_t* const p_row0 = smem + LY::kPOff + row * 128;
+    uint32_t it = 0;
+    int n = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      float m_used = -INFINITY, l_sum = 0.f;
+      bool ok = true;
+      for (int j = 0; j < I.nblk; ++j) {
+        const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+        ok = mbar_wait_bounded(&bars->s_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[kBlockN];
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c) EC_TMEM_LD32(tmem + lane_off + kTmemS + slot * kBlockN + c * 32, (sr + c * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bars->s_free[slot]);
+
+        const int nvalid = min(kBlockN, I.kv_end - (I.kb0 + j) * kBlockN);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) {
+          float s = __uint_as_float(sr[c]) * scale_log2;
+          if (c >= nvalid) s = -INFINITY;
+          sr[c] = __float_as_uint(s);
+          mx = fmaxf(mx, s);
+        }
+        bool rescale = false;
+        float alpha = 1.f;
+        if (j == 0) {
+          m_used = mx;
+        } else if (mx > m_used + kRescaleLog2) {
+          alpha = ex2_approx(m_used - mx);
+          m_used = mx;
+          l_sum *= alpha;
+          rescale = true;
+        }
+        float rs = 0.f;
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 2) {
+          const float p0 = ex2_approx(__uint_as_float(sr[c]) - m_used);
+          const float p1 = ex2_approx(__uint_as_float(sr[c + 1]) - m_used);
+          rs += p0 + p1;
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+        l_sum += rs;
+        ok = mbar_wait_bounded(&bars->p_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
+        if (!ok) break;
+        uint8_t* prow = p_row0 + slot * LY::kPBytes;
+#pragma unroll
+        for (int c = 0; c < kBlockN / 8; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
+          const int atom = c >> 3, ch = c & 7;
+          uint4 v;
+          v.x = pk[4 * c + 0];
+          v.y = pk[4 * c + 1];
+          v.z = pk[4 * c + 2];
+          v.w = pk[4 * c + 3];
+          *reinterpret_cast<uint4*>(prow + atom * LY::kAtomBytes + ((ch ^ (row & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        if (rescale) {
+          // O holds the products of blocks 0 .. j-1; wait for the last of them, then scale.
+          ok = mbar_wait_bounded(&bars->pv_done, (cur - 1) & 1u, abort_flag, dev_err, kWaitLimitNs);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            EC_TMEM_ST32(tmem + lane_off + kTmemO + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[slot]);
+      }
+      it += I.nblk;
+      if (ok) ok = mbar_wait_bounded(&bars->o_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
+      const int rl = row / g, jh = row - rl * g;
+      const bool valid_row = ok && row < M_rows && rl < I.nrows;
+      const int r = I.r0 + rl;
+      const int h = I.kvh * g + jh;
+      if (ok) {
+        tc_fence_after();
+        if (pl.splits == 1) {
+          const float inv_l = 1.f / l_sum;
+          uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + r) * Hq + h) * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
+            tmem_wait_ld();
+            if (valid_row) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+                *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = v;
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);
+        } else {
+          // Unnormalised partial of this split: O row, running max (log2 units), running sum.
+          float* slot_base = part + static_cast<int64_t>(item) * (kBlockM * (D + 2));
+          float* prow_o = slot_base + row * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<float4*>(prow_o + c * 32 + 4 * q) =
+                  make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                              __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+          }
+          slot_base[kBlockM * D + row] = m_used;
+          slot_base[kBlockM * D + kBlockM + row] = l_sum;
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);
+          __threadfence();
+          named_bar_sync(1, 128);
+          if (threadIdx.x == 64) {
+            const uint32_t done = atomicAdd(counters + I.tile, 1u);
+            bars->last_flag = (done == static_cast<uint32_t>(pl.splits - 1)) ? 1 : 0;
+          }
+          named_bar_sync(1, 128);
+          if (bars->last_flag) {
+            __threadfence();
+            const float* tile_base = part + static_cast<int64_t>(I.tile) * pl.splits * (kBlockM * (D + 2));
+            float mmax = -INFINITY;
+            for (int sp = 0; sp < pl.splits; ++sp)
+              mmax = fmaxf(mmax, __ldcg(tile_base + sp * (kBlockM * (D + 2)) + kBlockM * D + row));
+            float lsum = 0.f;
+            for (int sp = 0; sp < pl.splits; ++sp) {
+              const float* sb = tile_base + sp * (kBlockM * (D + 2));
+              lsum += ex2_approx(__ldcg(sb + kBlockM * D + row) - mmax) * __ldcg(sb + kBlockM * D + kBlockM + row);
+            }
+            const float inv_l = 1.f / lsum;
+            uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + r) * Hq + h) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              float acc[32];
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+              for (int sp = 0; sp < pl.splits; ++sp) {
+                const float* sb = tile_base + sp * (kBlockM * (D + 2));
+                const float f = ex2_approx(__ldcg(sb + kBlockM * D + row) - mmax) * inv_l;
+                const float4* src = reinterpret_cast<const float4*>(sb + row * D + c * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 v = __ldcg(src + q);
+                  acc[4 * q + 0] = fmaf(f, v.x, acc[4 * q + 0]);
+                  acc[4 * q + 1] = fmaf(f, v.y, acc[4 * q + 1]);
+                  acc[4 * q + 2] = fmaf(f, v.z, acc[4 * q + 2]);
+                  acc[4 * q + 3] = fmaf(f, v.w, acc[4 * q + 3]);
+                }
+              }
+              if (valid_row) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  uint4 v;
+                  v.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
+                  v.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
+                  v.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
+                  v.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
+                  *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = v;
+                }
+              }
+            }
+            if (threadIdx.x == 64) counters[I.tile] = 0u;
+          }
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  // ---------------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------- host
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                         dims, strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* R, float scale, void* out, void* ws, int32_t* dev_err, cudaStream_t s,
+                        ec_status* status) {
+  using LY = Layout<D>;
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) {
+    *status = EC_ERR_CUDA;
+    return cudaErrorNotSupported;
+  }
+  const int g = p.Hq / p.Hkv;
+  const int nr = kBlockM / g;
+  CUtensorMap tq, tk, tv;
+  const cuuint64_t qd[5] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(g), static_cast<cuuint64_t>(p.Hkv),
+                            static_cast<cuuint64_t>(p.L), static_cast<cuuint64_t>(p.B)};
+  const cuuint64_t qs[4] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(g) * D * 2,
+                            static_cast<cuuint64_t>(p.Hq) * D * 2, static_cast<cuuint64_t>(p.L) * p.Hq * D * 2};
+  const cuuint32_t qb[5] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(nr), 1};
+  const cuuint64_t kd[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.Hkv), static_cast<cuuint64_t>(p.L),
+                            static_cast<cuuint64_t>(p.B)};
+  const cuuint64_t ks[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(p.Hkv) * D * 2,
+                            static_cast<cuuint64_t>(p.L) * p.Hkv * D * 2};
+  const cuuint32_t kb[4] = {64, 1, static_cast<cuuint32_t>(kBlockN), 1};
+  if (!encode_map(enc, &tq, q, 5, qd, qs, qb) || !encode_map(enc, &tk, k_cache, 4, kd, ks, kb) ||
+      !encode_map(enc, &tv, v_cache, 4, kd, ks, kb)) {
+    *status = EC_ERR_INVALID_ARG;
+    return cudaErrorInvalidValue;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    *status = EC_ERR_CUDA;
+    return e;
+  }
+  static bool configured = false;
+  if (!configured) {
+    e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kDynSmem);
+    if (e != cudaSuccess) {
+      *status = EC_ERR_CUDA;
+      return e;
+    }
+    configured = true;
+  }
+  const int grid = std::min(sms, kMaxGrid);
+  float* part = static_cast<float*>(ws);
+  auto* counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) +
+                                               align_up(static_cast<size_t>(kMaxGrid) * kBlockM * (D + 2) * 4, 256));
+  attention_kernel<D><<<grid, kThreads, LY::kDynSmem, s>>>(tq, tk, tv, R, p.B, p.L, p.Hq, p.Hkv, g, nr,
+                                                           scale * kLog2e, static_cast<uint16_t*>(out), part,
+                                                           counters, dev_err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *status = EC_ERR_CUDA;
+  return e;
+}
+
+}  // namespace
+
+size_t attention_workspace_bytes(const ec_params& p) {
+  const size_t d = static_cast<size_t>(p.D);
+  return align_up(static_cast<size_t>(kMaxGrid) * kBlockM * (d + 2) * 4, 256) +
+         align_up(static_cast<size_t>(kMaxGrid) * sizeof(uint32_t), 256);
+}
+
+cudaError_t launch_partial_attention(const ec_params& p, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
+                                     int32_t* dev_err, cudaStream_t s, ec_status* status) {
+  *status = EC_OK;
+  if (p.D == 128) return launch_impl<128>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, s, status);
+  return launch_impl<64>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, s, status);
+}
+
+}  // namespace ec

@@ -1,0 +1,241 @@
+// ec_api.cu — the C ABI of the EntropyCache step library: host-side validation, workspace
+// layout and the composition of the stages into one denoising step.
+//
+// Every entry point validates its arguments on the host before launching anything, returns
+// an ec_status and never throws. The library allocates no memory.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "ec_internal.h"
+#include "entropycache.h"
+
+using namespace ec;
+
+namespace {
+
+constexpr int32_t kMaxB = 4096;
+constexpr int32_t kMaxL = 1 << 20;
+constexpr int32_t kMaxV = 1 << 30;
+constexpr int32_t kMaxCmax = 1024;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EC_OK : EC_ERR_CUDA; }
+
+// Shape checks common to the stages that need them. `what` selects the groups checked.
+enum : int { kCheckDecode = 1, kCheckSelect = 2, kCheckAttn = 4 };
+
+ec_status check_params(const ec_params* p, int what) {
+  if (p == nullptr) return EC_ERR_INVALID_ARG;
+  if (p->B < 1 || p->B > kMaxB || p->L < 1 || p->L > kMaxL) return EC_ERR_INVALID_ARG;
+  if (what & kCheckDecode) {
+    if (p->V < 1 || p->V > kMaxV) return EC_ERR_INVALID_ARG;
+    if (p->logits_dtype != EC_F32 && p->logits_dtype != EC_BF16) return EC_ERR_INVALID_ARG;
+  }
+  if (what & kCheckSelect) {
+    if (p->C_max < 1 || p->C_max > std::min(p->L, kMaxCmax)) return EC_ERR_INVALID_ARG;
+    if (p->k < 1 || p->k > p->L) return EC_ERR_INVALID_ARG;
+    if (p->n_dec < 1 || p->n_dec > p->C_max) return EC_ERR_INVALID_ARG;
+    if (p->tau != p->tau) return EC_ERR_INVALID_ARG;  // NaN threshold
+  }
+  if (what & kCheckAttn) {
+    if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0) return EC_ERR_INVALID_ARG;
+    if (p->Hq / p->Hkv > 128) return EC_ERR_UNSUPPORTED;
+    if (p->D != 64 && p->D != 128) return EC_ERR_UNSUPPORTED;
+    const int64_t g = p->Hq / p->Hkv;
+    const int64_t nr = 128 / g;
+    const int64_t tiles = static_cast<int64_t>(p->B) * p->Hkv * ((p->L + nr - 1) / nr);
+    if (tiles > (1ll << 30)) return EC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(p->Hq) * p->D * p->L * p->B > (1ll << 40)) return EC_ERR_UNSUPPORTED;
+  }
+  return EC_OK;
+}
+
+ec_status check_state(const ec_state* st) {
+  if (st == nullptr) return EC_ERR_INVALID_ARG;
+  if (!st->tokens || !st->mask || !st->ring || !st->ring_head || !st->ring_count || !st->dec_pos || !st->E ||
+      !st->flag || !st->idx || !st->R)
+    return EC_ERR_INVALID_ARG;
+  return EC_OK;
+}
+
+// ---- ec_step workspace layout --------------------------------------------------------
+struct StepLayout {
+  size_t k1, ids, ent, conf, qbuf, attn, total;
+};
+
+StepLayout step_layout(const ec_params& p) {
+  StepLayout s{};
+  const size_t rows = static_cast<size_t>(p.B) * p.C_max;
+  size_t off = 0;
+  s.k1 = off;
+  off += align_up(entropy_workspace_bytes(static_cast<int32_t>(rows), p.V, p.logits_dtype), 256);
+  s.ids = off;
+  off += align_up(rows * 4, 256);
+  s.ent = off;
+  off += align_up(rows * 4, 256);
+  s.conf = off;
+  off += align_up(rows * 4, 256);
+  s.qbuf = off;
+  off += align_up(static_cast<size_t>(p.B) * p.L * p.Hq * p.D * 2, 256);
+  s.attn = off;
+  off += align_up(attention_workspace_bytes(p), 256);
+  s.total = off;
+  return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ec_status_string(ec_status st) {
+  switch (st) {
+    case EC_OK: return "EC_OK";
+    case EC_ERR_INVALID_ARG: return "EC_ERR_INVALID_ARG";
+    case EC_ERR_UNSUPPORTED: return "EC_ERR_UNSUPPORTED";
+    case EC_ERR_CUDA: return "EC_ERR_CUDA";
+    case EC_ERR_DEVICE_CHECK: return "EC_ERR_DEVICE_CHECK";
+    case EC_ERR_TIMEOUT: return "EC_ERR_TIMEOUT";
+    default: return "EC_ERR_UNKNOWN";
+  }
+}
+
+int32_t ec_version(void) { return 100; }
+
+ec_status ec_read_device_error(const int32_t* dev_err, int32_t* host_word, ec_stream_t stream) {
+  if (dev_err == nullptr) return EC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t w = 0;
+  cudaError_t e = cudaMemcpyAsync(&w, dev_err, sizeof(w), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return EC_ERR_CUDA;
+  if (host_word != nullptr) *host_word = w;
+  if (w == 0) return EC_OK;
+  return (w & EC_DEVERR_TIMEOUT) ? EC_ERR_TIMEOUT : EC_ERR_DEVICE_CHECK;
+}
+
+// ---- (a) ----------------------------------------------------------------------------------
+size_t ec_entropy_decode_workspace_size(int32_t n_rows, int32_t V, int32_t dtype) {
+  if (n_rows < 0 || V < 1 || V > kMaxV || (dtype != EC_F32 && dtype != EC_BF16)) return 0;
+  return entropy_workspace_bytes(n_rows, V, dtype);
+}
+
+ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V, int32_t dtype,
+                            int32_t* ids, float* entropy, float* log_conf, void* ws, size_t ws_bytes,
+                            ec_stream_t stream) {
+  if (dtype != EC_F32 && dtype != EC_BF16) return EC_ERR_INVALID_ARG;
+  if (V < 1 || V > kMaxV || n_rows < 0 || row_stride < V) return EC_ERR_INVALID_ARG;
+  if (n_rows == 0) return EC_OK;
+  const int64_t esize = dtype == EC_F32 ? 4 : 2;
+  if ((row_stride * esize) % 16 != 0) return EC_ERR_INVALID_ARG;
+  if (!logits || !ids || !entropy || !log_conf || !aligned16(logits)) return EC_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(n_rows) * entropy_num_chunks(V, dtype) > INT32_MAX) return EC_ERR_UNSUPPORTED;
+  const size_t need = entropy_workspace_bytes(n_rows, V, dtype);
+  if (entropy_num_chunks(V, dtype) > 1 && (ws == nullptr || ws_bytes < need || !aligned16(ws)))
+    return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf, ws,
+                                           nullptr, 1, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- (b)+(c) --------------------------------------------------------------------------------
+ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int32_t* cand_pos,
+                              const int32_t* cand_count, const int32_t* ids, const float* entropy,
+                              const float* log_conf, ec_stream_t stream) {
+  ec_status r = check_params(p, kCheckSelect);
+  if (r != EC_OK) return r;
+  if ((r = check_state(st)) != EC_OK) return r;
+  if (!cand_pos || !cand_count || !ids || !entropy || !log_conf) return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_select_recompute(*p, *st, cand_pos, cand_count, ids, entropy, log_conf,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+// ---- (c) scatter ------------------------------------------------------------------------------
+ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                        int32_t src_by_position, const int32_t* idx, const int32_t* R, int32_t* dev_err,
+                        ec_stream_t stream) {
+  if (p == nullptr) return EC_ERR_INVALID_ARG;
+  if (p->B < 1 || p->B > kMaxB || p->L < 1 || p->L > kMaxL || p->Hkv < 1) return EC_ERR_INVALID_ARG;
+  if (p->D != 64 && p->D != 128) return EC_ERR_UNSUPPORTED;
+  if (src_by_position != 0 && src_by_position != 1) return EC_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || !k_new || !v_new || !idx || !R) return EC_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+    return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_kv_scatter(*p, k_cache, v_cache, k_new, v_new, src_by_position, idx, R, nullptr,
+                                       nullptr, dev_err, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- (d) ----------------------------------------------------------------------------------------
+size_t ec_partial_attention_workspace_size(const ec_params* p) {
+  if (check_params(p, kCheckAttn) != EC_OK) return 0;
+  return attention_workspace_bytes(*p);
+}
+
+ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* R, float scale, void* out, void* ws, size_t ws_bytes,
+                               int32_t* dev_err, ec_stream_t stream) {
+  ec_status r = check_params(p, kCheckAttn);
+  if (r != EC_OK) return r;
+  if (!q || !k_cache || !v_cache || !R || !out || !ws) return EC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(ws))
+    return EC_ERR_INVALID_ARG;
+  if (ws_bytes < attention_workspace_bytes(*p)) return EC_ERR_INVALID_ARG;
+  if (!(scale == scale)) return EC_ERR_INVALID_ARG;
+  ec_status st = EC_OK;
+  launch_partial_attention(*p, q, k_cache, v_cache, R, scale, out, ws, dev_err, static_cast<cudaStream_t>(stream),
+                           &st);
+  return st;
+}
+
+// ---- whole step ---------------------------------------------------------------------------------
+size_t ec_step_workspace_size(const ec_params* p) {
+  if (check_params(p, kCheckDecode | kCheckSelect | kCheckAttn) != EC_OK) return 0;
+  return step_layout(*p).total;
+}
+
+ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, const int32_t* cand_pos,
+                  const int32_t* cand_count, int32_t n_layers, void* const* k_cache, void* const* v_cache,
+                  const void* const* k_src, const void* const* v_src, const void* const* q_src, void* const* out,
+                  float scale, void* ws, size_t ws_bytes, ec_stream_t stream) {
+  ec_status r = check_params(p, kCheckDecode | kCheckSelect | kCheckAttn);
+  if (r != EC_OK) return r;
+  if ((r = check_state(st)) != EC_OK) return r;
+  const int64_t esize = p->logits_dtype == EC_F32 ? 4 : 2;
+  if ((static_cast<int64_t>(p->V) * esize) % 16 != 0) return EC_ERR_INVALID_ARG;
+  if (!logits || !aligned16(logits) || !cand_pos || !cand_count || !ws || !aligned16(ws)) return EC_ERR_INVALID_ARG;
+  if (n_layers < 0 || (n_layers > 0 && (!k_cache || !v_cache || !k_src || !v_src || !q_src || !out)))
+    return EC_ERR_INVALID_ARG;
+  if (!(scale == scale)) return EC_ERR_INVALID_ARG;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    if (!k_cache[l] || !v_cache[l] || !k_src[l] || !v_src[l] || !q_src[l] || !out[l]) return EC_ERR_INVALID_ARG;
+    if (!aligned16(k_cache[l]) || !aligned16(v_cache[l]) || !aligned16(k_src[l]) || !aligned16(v_src[l]) ||
+        !aligned16(q_src[l]) || !aligned16(out[l]))
+      return EC_ERR_INVALID_ARG;
+  }
+  const StepLayout lay = step_layout(*p);
+  if (ws_bytes < lay.total) return EC_ERR_INVALID_ARG;
+  char* w = static_cast<char*>(ws);
+  auto* ids = reinterpret_cast<int32_t*>(w + lay.ids);
+  auto* ent = reinterpret_cast<float*>(w + lay.ent);
+  auto* conf = reinterpret_cast<float*>(w + lay.conf);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  const int32_t rows = p->B * p->C_max;
+  cudaError_t e = launch_entropy_decode(logits, p->V, rows, p->V, p->logits_dtype, ids, ent, conf, w + lay.k1,
+                                        cand_count, p->C_max, s);
+  if (e != cudaSuccess) return EC_ERR_CUDA;
+  e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, s);
+  if (e != cudaSuccess) return EC_ERR_CUDA;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    e = launch_kv_scatter(*p, k_cache[l], v_cache[l], k_src[l], v_src[l], 1, st->idx, st->R, q_src[l],
+                          w + lay.qbuf, st->dev_err, s);
+    if (e != cudaSuccess) return EC_ERR_CUDA;
+    ec_status as = EC_OK;
+    launch_partial_attention(*p, w + lay.qbuf, k_cache[l], v_cache[l], st->R, scale, out[l], w + lay.attn,
+                             st->dev_err, s, &as);
+    if (as != EC_OK) return as;
+  }
+  return EC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// ec_internal.h — launchers shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "entropycache.h"
+
+namespace ec {
+
+// ---- entropy_decode ---------------------------------------------------------------------
+// Partial result of one vocabulary chunk of one row: raw max logit, its (lowest) index, and
+// S = sum 2^d, T = sum d 2^d with d = (x - max) * log2(e).
+struct ChunkPartial {
+  float m;
+  int32_t idx;
+  float s;
+  float t;
+};
+
+int entropy_chunk_elems(int32_t dtype);
+int32_t entropy_num_chunks(int32_t V, int32_t dtype);
+size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype);
+// row_count (may be null): rows r with (r % rows_per_group) >= row_count[r / rows_per_group]
+// are skipped (their outputs are left untouched).
+cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
+                                  int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
+                                  const int32_t* row_count, int32_t rows_per_group, cudaStream_t s);
+
+// ---- select_recompute ---------------------------------------------------------------------
+cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
+                                    const int32_t* cand_count, const int32_t* ids, const float* entropy,
+                                    const float* log_conf, cudaStream_t s);
+
+// ---- kv_scatter (+ optional query gather) -------------------------------------------------
+cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, const void* k_new,
+                              const void* v_new, int32_t src_by_position, const int32_t* idx,
+                              const int32_t* R, const void* q_src, void* q_dst, int32_t* dev_err,
+                              cudaStream_t s);
+
+// ---- partial attention --------------------------------------------------------------------
+size_t attention_workspace_bytes(const ec_params& p);
+cudaError_t launch_partial_attention(const ec_params& p, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
+                                     int32_t* dev_err, cudaStream_t s, ec_status* status);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace ec

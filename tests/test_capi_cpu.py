@@ -1,0 +1,167 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared entry point,
+reports workspace sizes, and rejects bad arguments on the host before any launch.
+
+The pointers used below are never dereferenced on the host: every call here fails
+validation before it reaches CUDA.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from entropy_gated_kv_gb300 import build as B
+
+    B.build()
+    from entropy_gated_kv_gb300 import _capi as C
+
+    C.load()
+    return C
+
+
+def header_functions() -> list[str]:
+    text = (ROOT / "include" / "entropycache.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ec_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(capi):
+    names = header_functions()
+    assert len(names) >= 10
+    lib = capi.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(capi.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings(capi):
+    lib = capi.load()
+    assert lib.ec_status_string(0) == b"EC_OK"
+    assert lib.ec_status_string(capi.EC_ERR_INVALID_ARG) == b"EC_ERR_INVALID_ARG"
+    assert lib.ec_status_string(capi.EC_ERR_TIMEOUT) == b"EC_ERR_TIMEOUT"
+    assert lib.ec_status_string(999) == b"EC_ERR_UNKNOWN"
+    assert lib.ec_version() >= 100
+
+
+def _params(C, **kw):
+    base = dict(B=1, L=1024, Hq=32, Hkv=32, D=128, V=126464, C_max=32, k=64, n_dec=1, tau=1.0, logits_dtype=C.EC_BF16)
+    base.update(kw)
+    return C.EcParams(**base)
+
+
+def test_workspace_sizes(capi):
+    lib = capi.load()
+    # one vocabulary chunk per CTA: 8192 bf16 / 4096 fp32 elements
+    assert lib.ec_entropy_decode_workspace_size(32, 126464, capi.EC_BF16) >= 32 * 16 * 16
+    assert lib.ec_entropy_decode_workspace_size(32, 32000, capi.EC_F32) >= 32 * 8 * 16
+    assert lib.ec_entropy_decode_workspace_size(-1, 10, capi.EC_F32) == 0
+    assert lib.ec_entropy_decode_workspace_size(1, 10, 7) == 0
+    p = _params(capi)
+    a = lib.ec_partial_attention_workspace_size(ctypes.byref(p))
+    s = lib.ec_step_workspace_size(ctypes.byref(p))
+    assert a > 0 and s > a + 1024 * 32 * 128 * 2
+    bad = _params(capi, D=96)
+    assert lib.ec_partial_attention_workspace_size(ctypes.byref(bad)) == 0
+    assert lib.ec_step_workspace_size(ctypes.byref(bad)) == 0
+
+
+FAKE = 0x100000  # an aligned address that is never dereferenced
+
+
+def test_entropy_decode_rejects_bad_args(capi):
+    lib = capi.load()
+    f = lib.ec_entropy_decode
+    p = ctypes.c_void_p(FAKE)
+    INV = capi.EC_ERR_INVALID_ARG
+    assert f(p, 32000, 4, 32000, 7, p, p, p, p, 1 << 20, None) == INV  # dtype
+    assert f(p, 100, 4, 200, capi.EC_F32, p, p, p, p, 1 << 20, None) == INV  # stride < V
+    assert f(p, 32001, 4, 32000, capi.EC_F32, p, p, p, p, 1 << 20, None) == INV  # stride*4 % 16
+    assert f(p, 50257, 4, 50257, capi.EC_BF16, p, p, p, p, 1 << 20, None) == INV  # stride*2 % 16
+    assert f(None, 32000, 4, 32000, capi.EC_F32, p, p, p, p, 1 << 20, None) == INV
+    assert f(ctypes.c_void_p(FAKE + 4), 32000, 4, 32000, capi.EC_F32, p, p, p, p, 1 << 20, None) == INV
+    assert f(p, 32000, 4, 32000, capi.EC_F32, p, p, p, None, 0, None) == INV  # workspace
+    assert f(p, 32000, 4, 32000, capi.EC_F32, p, p, p, p, 16, None) == INV  # workspace too small
+    assert f(p, 32000, -1, 32000, capi.EC_F32, p, p, p, p, 1 << 20, None) == INV
+    assert f(p, 32000, 0, 32000, capi.EC_F32, None, None, None, None, 0, None) == capi.EC_OK  # empty: no-op
+
+
+def test_partial_attention_rejects_bad_args(capi):
+    lib = capi.load()
+    f = lib.ec_partial_attention
+    p = ctypes.c_void_p(FAKE)
+    big = 1 << 30
+    good = _params(capi)
+    for bad, want in [
+        (_params(capi, Hkv=5), capi.EC_ERR_INVALID_ARG),  # Hq % Hkv
+        (_params(capi, D=96), capi.EC_ERR_UNSUPPORTED),
+        (_params(capi, Hq=256, Hkv=1), capi.EC_ERR_UNSUPPORTED),  # g > 128
+        (_params(capi, B=0), capi.EC_ERR_INVALID_ARG),
+        (_params(capi, L=0), capi.EC_ERR_INVALID_ARG),
+    ]:
+        assert f(ctypes.byref(bad), p, p, p, p, 0.1, p, p, big, None, None) == want
+    assert f(None, p, p, p, p, 0.1, p, p, big, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), None, p, p, p, 0.1, p, p, big, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), ctypes.c_void_p(FAKE + 8), p, p, p, 0.1, p, p, big, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), p, p, p, p, 0.1, p, p, 64, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), p, p, p, p, float("nan"), p, p, big, None, None) == capi.EC_ERR_INVALID_ARG
+
+
+def test_select_and_scatter_reject_bad_args(capi):
+    lib = capi.load()
+    p = ctypes.c_void_p(FAKE)
+    st = capi.EcState(*([p] * 11))
+    INV = capi.EC_ERR_INVALID_ARG
+    for bad in [dict(k=0), dict(k=2000), dict(n_dec=0), dict(n_dec=33), dict(C_max=0), dict(C_max=2048),
+                dict(tau=float("nan"))]:
+        pp = _params(capi, **bad)
+        assert lib.ec_select_recompute(ctypes.byref(pp), ctypes.byref(st), p, p, p, p, p, None) == INV, bad
+    good = _params(capi)
+    st_missing = capi.EcState(*([p] * 10 + [None]))  # dev_err may be NULL ...
+    st_bad = capi.EcState(*([None] + [p] * 10))  # ... tokens may not
+    assert lib.ec_select_recompute(ctypes.byref(good), ctypes.byref(st_bad), p, p, p, p, p, None) == INV
+    assert lib.ec_select_recompute(ctypes.byref(good), None, p, p, p, p, p, None) == INV
+    assert lib.ec_select_recompute(ctypes.byref(good), ctypes.byref(st_missing), None, p, p, p, p, None) == INV
+    sc = lib.ec_kv_scatter
+    assert sc(ctypes.byref(_params(capi, D=80)), p, p, p, p, 0, p, p, None, None) == capi.EC_ERR_UNSUPPORTED
+    assert sc(ctypes.byref(good), p, p, p, p, 2, p, p, None, None) == INV
+    assert sc(ctypes.byref(good), p, ctypes.c_void_p(FAKE + 2), p, p, 0, p, p, None, None) == INV
+    assert sc(ctypes.byref(good), p, p, p, p, 0, None, p, None, None) == INV
+
+
+def test_step_rejects_bad_args(capi):
+    lib = capi.load()
+    p = ctypes.c_void_p(FAKE)
+    st = capi.EcState(*([p] * 11))
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    good = _params(capi)
+    big = 1 << 34
+    f = lib.ec_step
+    args = lambda pp, n=1, ws=p, wsb=big: (ctypes.byref(pp), ctypes.byref(st), p, p, p, n, arr, arr, arr, arr, arr, arr,  # noqa: E731
+                                           0.088, ws, wsb, None)
+    assert f(*args(_params(capi, V=50257))) == capi.EC_ERR_INVALID_ARG  # V*2 % 16 for the packed logits
+    assert f(*args(good, n=-1)) == capi.EC_ERR_INVALID_ARG
+    assert f(*args(good, wsb=1024)) == capi.EC_ERR_INVALID_ARG
+    assert f(*args(good, ws=None)) == capi.EC_ERR_INVALID_ARG
+    null_arr = (ctypes.c_void_p * 1)(0)
+    a = list(args(good))
+    a[6] = null_arr
+    assert f(*a) == capi.EC_ERR_INVALID_ARG
+
+
+def test_read_device_error_rejects_null(capi):
+    lib = capi.load()
+    assert lib.ec_read_device_error(None, None, None) == capi.EC_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(capi):
+    import torch
+
+    import entropy_gated_kv_gb300 as E
+
+    with pytest.raises(ValueError):
+        E.entropy_decode(torch.zeros(2, 64))

@@ -20,11 +20,15 @@
 // Grouped-query attention packs the g = Hq / Hkv query heads of one KV head into the 128 MMA
 // rows (floor(128 / g) query rows per tile), so K/V are read once per KV head.
 // Work items (b, kv head, row tile, KV split) are derived on the device from R[], so the
-// kernel needs no host synchronisation. When there are fewer row tiles than CTAs the key
-// range is split; each split writes an unnormalised partial (O, running max, running sum)
-// and the last split to finish (a counter per tile, no spinning) merges them by
-// log-sum-exp weights — the split-KV-then-merge idea of "Prefilling-dLLM" (gist.science pt
-// summary, "Otimização de Kernel de Atenção").
+// kernel needs no host synchronisation. CTAs are launched in clusters of 4. When there are
+// no more row tiles than clusters (a partial step), the 4 CTAs of a cluster share one tile and
+// each takes a quarter of the key range; each stages its unnormalised partial (O, running max,
+// running sum) in its own shared memory; after a cluster barrier each CTA pushes every peer
+// the 32 rows that peer merges with one bulk shared-to-shared copy (the async copy engine,
+// completion counted on the peer's mbarrier), and merges its own 32 rows by log-sum-exp
+// weights from local shared memory — the split-KV-then-merge idea of "Prefilling-dLLM"
+// (gist.science pt summary, "Otimização de Kernel de Atenção"), with the merge kept on chip. Otherwise (a full step)
+// every CTA works through whole tiles on its own.
 #include <cuda.h>
 
 #include <algorithm>
@@ -45,6 +49,7 @@ constexpr uint32_t kTmemO = 256;  // O accumulator at columns [256, 256 + D)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxGrid = 256;
+constexpr int kCluster = 4;  // CTAs per cluster = KV splits of a shared tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
 struct Bars {
@@ -53,9 +58,9 @@ struct Bars {
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_free[2];
   uint64_t pv_done, o_full, o_free;
+  uint64_t recv;  // split merge: bytes pushed into this CTA by its cluster peers
   uint32_t tmem_base;
   int abort;
-  int last_flag;
 };
 
 template <int D>
@@ -93,8 +98,9 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-// Whole warp; every warp of every CTA computes the same plan.
-__device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int grid) {
+// Whole warp; every warp of every CTA computes the same plan. With no more tiles than
+// clusters, each cluster shares one tile over kCluster key splits; otherwise no split.
+__device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int nclusters) {
   const int lane = threadIdx.x & 31;
   int t = 0;
   for (int b = lane; b < B; b += 32) t += Hkv * ((clamp_r(__ldg(R + b), L) + nr - 1) / nr);
@@ -102,11 +108,18 @@ __device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int g
   Plan p;
   p.tiles = t;
   p.nkv = (L + kBlockN - 1) / kBlockN;
-  int s = 1;
-  if (t > 0 && t < grid) s = min(p.nkv, grid / t);
+  const int s = (t > 0 && t <= nclusters) ? min(kCluster, p.nkv) : 1;
   p.bps = (p.nkv + s - 1) / s;
   p.splits = (p.nkv + p.bps - 1) / p.bps;
   return p;
+}
+
+// The k-th work item of this CTA, or -1. Split plans give cluster c the tile c and its CTA of
+// rank r the split r; unsplit plans deal tiles round-robin over all CTAs.
+__device__ __forceinline__ int cta_item(int k, const Plan& pl, int cluster, int rank, int nclusters) {
+  if (pl.splits > 1) return (k == 0 && cluster < pl.tiles && rank < pl.splits) ? cluster * pl.splits + rank : -1;
+  const int item = static_cast<int>(blockIdx.x) + k * static_cast<int>(gridDim.x);
+  return item < pl.tiles ? item : -1;
 }
 
 // Whole warp. Items are ordered (b, kv head, row tile, split).
@@ -155,15 +168,27 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Hq, int Hkv, int g,
-    int nr, float scale_log2, uint16_t* __restrict__ out, float* __restrict__ part, uint32_t* __restrict__ counters,
-    int32_t* __restrict__ dev_err) {
+    int nr, float scale_log2, uint16_t* __restrict__ out, int32_t* __restrict__ dev_err) {
   using LY = Layout<D>;
+  constexpr int kRedStride = D + 4;  // fp32 row stride of the staged partial (16-byte padded)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + LY::kBarOff);
   uint8_t* q_smem = smem + LY::kQOff;
+  // Split partials reuse the K/V stages and P buffers once every CTA of the cluster is past
+  // its compute: `send` holds this CTA's 128 partial rows (D values, then the running max and
+  // running sum in the row's padding), grouped by the peer that merges them; `recv` holds
+  // the kBlockM / kCluster rows this CTA merges, one slice per peer.
+  constexpr int kSliceRows = kBlockM / kCluster;
+  constexpr uint32_t kSliceBytes = kSliceRows * kRedStride * 4;
+  float* send = reinterpret_cast<float*>(smem + LY::kStageOff);
+  float* recv = send + kBlockM * kRedStride;
+  static_assert(LY::kStageOff + 2 * kBlockM * kRedStride * 4 <= LY::kBarOff, "split buffers overlap barriers");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M_rows = nr * g;
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int nclusters = static_cast<int>(cluster_count_x());
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -179,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, 128);
+    mbar_init(&bars->recv, 1);
     bars->abort = 0;
-    bars->last_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -198,14 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
 
-  const Plan pl = make_plan(R, B, L, Hkv, nr, gridDim.x);
-  const int n_items = pl.tiles * pl.splits;
+  // Everything above overlaps the previous kernel; R, Q and the cache are read from here on.
+  pdl_wait();
+  pdl_launch_dependents();
+  const Plan pl = make_plan(R, B, L, Hkv, nr, nclusters);
+  const bool split_mode = pl.splits > 1;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     uint32_t it = 0;
-    int n = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+    for (int n = 0;; ++n) {
+      const int item = cta_item(n, pl, cluster, rank, nclusters);
+      if (item < 0) break;
       const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
       int ok = 1;
       if (lane == 0) {
@@ -238,8 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
     const uint32_t q_addr = smem_u32(q_smem);
     uint32_t it = 0;
-    int n = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+    for (int n = 0;; ++n) {
+      const int item = cta_item(n, pl, cluster, rank, nclusters);
+      if (item < 0) break;
       const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
       int ok = 1;
       if (lane == 0) {
@@ -293,14 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     uint8_t* const p_row0 = smem + LY::kPOff + row * 128;
     uint32_t it = 0;
-    int n = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++n) {
+    bool staged = false;
+    for (int n = 0;; ++n) {
+      const int item = cta_item(n, pl, cluster, rank, nclusters);
+      if (item < 0) break;
       const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nblk; ++j) {
         const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
-        ok = mbar_wait_bounded(&bars->s_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
         uint32_t sr[kBlockN];
@@ -310,15 +342,22 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
         tc_fence_before();
         mbar_arrive(&bars->s_free[slot]);
 
+        // Row max of the raw scores (scale > 0 commutes with max), 8 independent chains.
         const int nvalid = min(kBlockN, I.kv_end - (I.kb0 + j) * kBlockN);
-        float mx = -INFINITY;
+        if (nvalid < kBlockN) {  // ragged last block of the key range
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) {
-          float s = __uint_as_float(sr[c]) * scale_log2;
-          if (c >= nvalid) s = -INFINITY;
-          sr[c] = __float_as_uint(s);
-          mx = fmaxf(mx, s);
+          for (int c = 0; c < kBlockN; ++c)
+            if (c >= nvalid) sr[c] = __float_as_uint(-INFINITY);
         }
+        float mxs[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mxs[e] = __uint_as_float(sr[e]);
+#pragma unroll
+        for (int c = 8; c < kBlockN; c += 8)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mxs[e] = fmaxf(mxs[e], __uint_as_float(sr[c + e]));
+        const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                               fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7]))) * scale_log2;
         bool rescale = false;
         float alpha = 1.f;
         if (j == 0) {
@@ -329,17 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
           l_sum *= alpha;
           rescale = true;
         }
-        float rs = 0.f;
+        // p = 2^(s * scale * log2(e) - m_used); row sum over 8 independent chains.
+        const float neg_m = -m_used;
+        float rss[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rss[e] = 0.f;
         uint32_t pk[kBlockN / 2];
 #pragma unroll
         for (int c = 0; c < kBlockN; c += 2) {
-          const float p0 = ex2_approx(__uint_as_float(sr[c]) - m_used);
-          const float p1 = ex2_approx(__uint_as_float(sr[c + 1]) - m_used);
-          rs += p0 + p1;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, neg_m));
+          rss[(c >> 1) & 7] += p0 + p1;
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
+        const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
         l_sum += rs;
-        ok = mbar_wait_bounded(&bars->p_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait_bounded(&bars->p_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs));
         if (!ok) break;
         uint8_t* prow = p_row0 + slot * LY::kPBytes;
 #pragma unroll
@@ -353,9 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
           *reinterpret_cast<uint4*>(prow + atom * LY::kAtomBytes + ((ch ^ (row & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
-        if (rescale) {
+        // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
+        // needs it (alpha = 1 for the others).
+        if (__any_sync(0xffffffffu, rescale)) {
           // O holds the products of blocks 0 .. j-1; wait for the last of them, then scale.
-          ok = mbar_wait_bounded(&bars->pv_done, (cur - 1) & 1u, abort_flag, dev_err, kWaitLimitNs);
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_bounded(&bars->pv_done, (cur - 1) & 1u, abort_flag, dev_err, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -374,109 +422,134 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       }
       it += I.nblk;
       if (ok) ok = mbar_wait_bounded(&bars->o_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
-      const int rl = row / g, jh = row - rl * g;
-      const bool valid_row = ok && row < M_rows && rl < I.nrows;
-      const int r = I.r0 + rl;
-      const int h = I.kvh * g + jh;
-      if (ok) {
-        tc_fence_after();
-        if (pl.splits == 1) {
-          const float inv_l = 1.f / l_sum;
-          uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + r) * Hq + h) * D;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      if (!split_mode) {
+        // Whole key range: normalise and write this row.
+        const int rl = row / g, jh = row - rl * g;
+        const bool valid_row = row < M_rows && rl < I.nrows;
+        const float inv_l = 1.f / l_sum;
+        uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + I.r0 + rl) * Hq + I.kvh * g + jh) * D;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
-            tmem_wait_ld();
-            if (valid_row) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
+          tmem_wait_ld();
+          if (valid_row) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-                v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
-                v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
-                v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-                *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = v;
-              }
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * q + 0]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = v;
             }
           }
-          tc_fence_before();
-          mbar_arrive(&bars->o_free);
-        } else {
-          // Unnormalised partial of this split: O row, running max (log2 units), running sum.
-          float* slot_base = part + static_cast<int64_t>(item) * (kBlockM * (D + 2));
-          float* prow_o = slot_base + row * D;
+        }
+      } else {
+        // One split of a shared tile: stage the unnormalised partial for the cluster merge.
+        // Every K/V load of this CTA has been consumed (o_full), so the stages are free.
+        float* ro = send + row * kRedStride;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<float4*>(prow_o + c * 32 + 4 * q) =
-                  make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
-                              __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(ro + c * 32 + 4 * q) =
+                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
+                            __uint_as_float(o[4 * q + 3]));
+        }
+        ro[D] = m_used;
+        ro[D + 1] = l_sum;
+        staged = true;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free);
+    }
+    if (split_mode && !staged) {  // no split of its own (or a failed one): contribute nothing
+      send[row * kRedStride + D] = -INFINITY;
+      send[row * kRedStride + D + 1] = 0.f;
+    }
+    if (split_mode) fence_proxy_async_smem();  // the bulk copies below read `send`
+  }
+
+  // ---------------------------------------------------------------------- cluster merge
+  if (split_mode) {
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&bars->recv, (kCluster - 1) * kSliceBytes);
+    cluster_sync_all();  // every CTA has staged its partial and armed its receive barrier
+    if (threadIdx.x == 0) {
+      // push each peer the slice of rows it merges (the own slice stays in `send`)
+      for (int d = 1; d < kCluster; ++d) {
+        const uint32_t dst = (rank + d) % kCluster;
+        const uint32_t dst_recv = dsmem_map(smem_u32(recv + rank * kSliceRows * kRedStride), dst);
+        bulk_copy_s2cluster(dst_recv, send + dst * kSliceRows * kRedStride, kSliceBytes,
+                            dsmem_map(smem_u32(&bars->recv), dst));
+      }
+    }
+    if (warp >= 2) {
+      const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->recv, 0, abort_flag, dev_err, kWaitLimitNs));
+      if (got && cluster < pl.tiles) {
+        const Item I = decode_item(cluster * pl.splits, pl, R, B, L, Hkv, nr);
+        constexpr int kCols = D / 4;  // four threads per row, kCols columns each
+        const int t = threadIdx.x - 64;
+        const int srow = t >> 2;  // row within this CTA's slice
+        const int prow = rank * kSliceRows + srow;
+        const int col0 = (t & 3) * kCols;
+        const float* src[kCluster];
+#pragma unroll
+        for (int sidx = 0; sidx < kCluster; ++sidx)
+          src[sidx] = (sidx == rank) ? send + prow * kRedStride : recv + (sidx * kSliceRows + srow) * kRedStride;
+        float wgt[kCluster], ls[kCluster];
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int sidx = 0; sidx < kCluster; ++sidx) {
+          wgt[sidx] = src[sidx][D];
+          ls[sidx] = src[sidx][D + 1];
+          if (ls[sidx] > 0.f) mmax = fmaxf(mmax, wgt[sidx]);
+        }
+        float lsum = 0.f;
+#pragma unroll
+        for (int sidx = 0; sidx < kCluster; ++sidx) {
+          wgt[sidx] = ls[sidx] > 0.f ? ex2_approx(wgt[sidx] - mmax) : 0.f;  // weight of split sidx
+          lsum = fmaf(wgt[sidx], ls[sidx], lsum);
+        }
+        const float inv_l = 1.f / lsum;
+        float acc[kCols];
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int sidx = 0; sidx < kCluster; ++sidx) {
+          if (wgt[sidx] == 0.f) continue;  // an empty split may hold stale values
+          const float4* o4 = reinterpret_cast<const float4*>(src[sidx] + col0);
+#pragma unroll
+          for (int q = 0; q < kCols / 4; ++q) {
+            const float4 v = o4[q];
+            acc[4 * q + 0] = fmaf(wgt[sidx], v.x, acc[4 * q + 0]);
+            acc[4 * q + 1] = fmaf(wgt[sidx], v.y, acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(wgt[sidx], v.z, acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(wgt[sidx], v.w, acc[4 * q + 3]);
           }
-          slot_base[kBlockM * D + row] = m_used;
-          slot_base[kBlockM * D + kBlockM + row] = l_sum;
-          tc_fence_before();
-          mbar_arrive(&bars->o_free);
-          __threadfence();
-          named_bar_sync(1, 128);
-          if (threadIdx.x == 64) {
-            const uint32_t done = atomicAdd(counters + I.tile, 1u);
-            bars->last_flag = (done == static_cast<uint32_t>(pl.splits - 1)) ? 1 : 0;
-          }
-          named_bar_sync(1, 128);
-          if (bars->last_flag) {
-            __threadfence();
-            const float* tile_base = part + static_cast<int64_t>(I.tile) * pl.splits * (kBlockM * (D + 2));
-            float mmax = -INFINITY;
-            for (int sp = 0; sp < pl.splits; ++sp)
-              mmax = fmaxf(mmax, __ldcg(tile_base + sp * (kBlockM * (D + 2)) + kBlockM * D + row));
-            float lsum = 0.f;
-            for (int sp = 0; sp < pl.splits; ++sp) {
-              const float* sb = tile_base + sp * (kBlockM * (D + 2));
-              lsum += ex2_approx(__ldcg(sb + kBlockM * D + row) - mmax) * __ldcg(sb + kBlockM * D + kBlockM + row);
-            }
-            const float inv_l = 1.f / lsum;
-            uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + r) * Hq + h) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              float acc[32];
+        }
+        const int rl = prow / g, jh = prow - rl * g;
+        if (prow < M_rows && rl < I.nrows && !*abort_flag) {
+          uint16_t* orow = out + ((static_cast<int64_t>(I.b) * L + I.r0 + rl) * Hq + I.kvh * g + jh) * D + col0;
 #pragma unroll
-              for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-              for (int sp = 0; sp < pl.splits; ++sp) {
-                const float* sb = tile_base + sp * (kBlockM * (D + 2));
-                const float f = ex2_approx(__ldcg(sb + kBlockM * D + row) - mmax) * inv_l;
-                const float4* src = reinterpret_cast<const float4*>(sb + row * D + c * 32);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 v = __ldcg(src + q);
-                  acc[4 * q + 0] = fmaf(f, v.x, acc[4 * q + 0]);
-                  acc[4 * q + 1] = fmaf(f, v.y, acc[4 * q + 1]);
-                  acc[4 * q + 2] = fmaf(f, v.z, acc[4 * q + 2]);
-                  acc[4 * q + 3] = fmaf(f, v.w, acc[4 * q + 3]);
-                }
-              }
-              if (valid_row) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  uint4 v;
-                  v.x = pack_bf16x2(acc[8 * q + 0], acc[8 * q + 1]);
-                  v.y = pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]);
-                  v.z = pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]);
-                  v.w = pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]);
-                  *reinterpret_cast<uint4*>(orow + c * 32 + 8 * q) = v;
-                }
-              }
-            }
-            if (threadIdx.x == 64) counters[I.tile] = 0u;
+          for (int q = 0; q < kCols / 8; ++q) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[8 * q + 0] * inv_l, acc[8 * q + 1] * inv_l);
+            v.y = pack_bf16x2(acc[8 * q + 2] * inv_l, acc[8 * q + 3] * inv_l);
+            v.z = pack_bf16x2(acc[8 * q + 4] * inv_l, acc[8 * q + 5] * inv_l);
+            v.w = pack_bf16x2(acc[8 * q + 6] * inv_l, acc[8 * q + 7] * inv_l);
+            *reinterpret_cast<uint4*>(orow + 8 * q) = v;
           }
         }
       }
-      if (!ok) break;
     }
+    cluster_sync_all();  // every push has landed and been read before any CTA leaves
   }
 
   // ---------------------------------------------------------------------- teardown
@@ -552,23 +625,42 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
     *status = EC_ERR_CUDA;
     return e;
   }
-  static bool configured = false;
-  if (!configured) {
+  // Clusters of kCluster CTAs, one CTA per SM (shared memory bound), as many clusters as
+  // fit on the device at once (the kernel is persistent).
+  static int max_clusters[2] = {0, 0};  // per head size
+  int& mc = max_clusters[D == 128 ? 1 : 0];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = LY::kDynSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
+  if (mc == 0) {
     e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kDynSmem);
     if (e != cudaSuccess) {
       *status = EC_ERR_CUDA;
       return e;
     }
-    configured = true;
+    cfg.gridDim = dim3(std::min(sms, kMaxGrid) / kCluster * kCluster);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, attention_kernel<D>, &cfg);
+    if (e != cudaSuccess || n < 1) {
+      *status = EC_ERR_CUDA;
+      return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+    }
+    mc = std::min(n, kMaxGrid / kCluster);
   }
-  const int grid = std::min(sms, kMaxGrid);
-  float* part = static_cast<float*>(ws);
-  auto* counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) +
-                                               align_up(static_cast<size_t>(kMaxGrid) * kBlockM * (D + 2) * 4, 256));
-  attention_kernel<D><<<grid, kThreads, LY::kDynSmem, s>>>(tq, tk, tv, R, p.B, p.L, p.Hq, p.Hkv, g, nr,
-                                                           scale * kLog2e, static_cast<uint16_t*>(out), part,
-                                                           counters, dev_err);
-  e = cudaGetLastError();
+  cfg.gridDim = dim3(mc * kCluster);
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, tq, tk, tv, R, p.B, p.L, p.Hq, p.Hkv, g, nr, scale * kLog2e,
+                         static_cast<uint16_t*>(out), dev_err);
   if (e != cudaSuccess) *status = EC_ERR_CUDA;
   return e;
 }
@@ -576,9 +668,8 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
 }  // namespace
 
 size_t attention_workspace_bytes(const ec_params& p) {
-  const size_t d = static_cast<size_t>(p.D);
-  return align_up(static_cast<size_t>(kMaxGrid) * kBlockM * (d + 2) * 4, 256) +
-         align_up(static_cast<size_t>(kMaxGrid) * sizeof(uint32_t), 256);
+  (void)p;
+  return 256;  // the split merge runs on chip; the workspace is reserved for future use
 }
 
 cudaError_t launch_partial_attention(const ec_params& p, const void* q, const void* k_cache,

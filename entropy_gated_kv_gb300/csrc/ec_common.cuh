@@ -207,3 +207,77 @@ EC_DEV void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 }  // namespace ec
+
+namespace ec {
+
+// ------------------------------------------------------------------------------------
+// thread-block clusters / distributed shared memory
+
+EC_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+EC_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+EC_DEV uint32_t cluster_count_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster (warp-aligned).
+EC_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in the CTA of the given rank.
+EC_DEV uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Remote loads are volatile (kept in program order after the cluster barrier) but carry no
+// memory clobber, so a run of them is issued back to back.
+EC_DEV float4 dsmem_ld_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+EC_DEV float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+}  // namespace ec
+
+namespace ec {
+
+// ------------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start while its predecessor in the stream is still running; it must call pdl_wait()
+// before touching anything the predecessor writes (the wait returns once the predecessor
+// has completed and its memory is visible).
+
+EC_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+EC_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+}  // namespace ec
+
+namespace ec {
+
+// Bulk copy from this CTA's shared memory to (possibly another CTA's) shared memory in the
+// cluster; completion is counted in bytes on the destination's mbarrier. Addresses 16-byte
+// aligned, size a multiple of 16.
+EC_DEV void bulk_copy_s2cluster(uint32_t dst_cluster_addr, const void* src, uint32_t bytes,
+                                uint32_t mbar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster_addr),
+      "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster_addr)
+      : "memory");
+}
+
+}  // namespace ec

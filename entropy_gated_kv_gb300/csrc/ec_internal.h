@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <utility>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -46,5 +47,28 @@ cudaError_t launch_partial_attention(const ec_params& p, const void* q, const vo
                                      int32_t* dev_err, cudaStream_t s, ec_status* status);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace ec
+
+namespace ec {
+
+// Launches `kernel` with programmatic stream serialization, so it may begin while the
+// previous kernel in the stream finishes; the kernel itself calls pdl_wait() before reading
+// its inputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace ec

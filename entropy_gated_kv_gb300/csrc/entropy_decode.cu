@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(kThreads) entropy_decode_kernel(
   const int64_t bid = blockIdx.x;
   const int row = static_cast<int>(bid / nchunks);
   const int chunk = static_cast<int>(bid - static_cast<int64_t>(row) * nchunks);
+  pdl_wait();  // logits and row counts may come from the previous kernel in the stream
+  pdl_launch_dependents();
   if (row_count != nullptr) {
     const int grp = row / rows_per_group;
     if (row - grp * rows_per_group >= __ldg(row_count + grp)) return;  // whole row skipped
@@ -337,16 +339,12 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   const int64_t nblocks = static_cast<int64_t>(n_rows) * nch;
   if (nblocks > INT_MAX) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(nblocks));
-  if (dtype == EC_F32) {
-    entropy_decode_kernel<EC_F32><<<grid, kThreads, 0, s>>>(
-        static_cast<const char*>(logits), row_stride * 4, V, nch, ids, entropy, log_conf, partials, counters,
-        row_count, rows_per_group);
-  } else {
-    entropy_decode_kernel<EC_BF16><<<grid, kThreads, 0, s>>>(
-        static_cast<const char*>(logits), row_stride * 2, V, nch, ids, entropy, log_conf, partials, counters,
-        row_count, rows_per_group);
-  }
-  return cudaGetLastError();
+  const char* lg = static_cast<const char*>(logits);
+  if (dtype == EC_F32)
+    return launch_pdl(entropy_decode_kernel<EC_F32>, grid, dim3(kThreads), 0, s, lg, row_stride * 4, V, nch, ids,
+                      entropy, log_conf, partials, counters, row_count, rows_per_group);
+  return launch_pdl(entropy_decode_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, lg, row_stride * 2, V, nch, ids,
+                    entropy, log_conf, partials, counters, row_count, rows_per_group);
 }
 
 }  // namespace ec

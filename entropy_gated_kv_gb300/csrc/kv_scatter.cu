@@ -8,9 +8,9 @@
 //   q_dst[b, r] = q_src[b, idx[b, r]]        (optional)
 //
 // A pure copy (HBM-bound, bytes = 2 reads + 2 writes of R * Hkv * D bf16, plus the query
-// rows). One warp per row; each lane moves 16-byte vectors, four loads in flight before the
-// stores. The grid is sized from L and the batch (R lives on the device) and warps stride
-// over the rows.
+// rows). One CTA per row with the whole row's loads in flight before its stores.
+#include <algorithm>
+
 #include "ec_common.cuh"
 #include "ec_internal.h"
 
@@ -18,7 +18,7 @@ namespace ec {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxVecPerThread = 8;  // 16-byte vectors held per thread before the stores
 
 __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
   uint4 r;
@@ -28,46 +28,53 @@ __device__ __forceinline__ uint4 ld_nc(const uint4* p) {
   return r;
 }
 
-// Copies n16 16-byte vectors from src to dst with the 32 lanes of a warp.
-__device__ __forceinline__ void warp_copy(uint4* __restrict__ dst, const uint4* __restrict__ src, int n16, int lane) {
-  int c = lane;
-  for (; c + 96 < n16; c += 128) {
-    const uint4 a = ld_nc(src + c), b2 = ld_nc(src + c + 32), d = ld_nc(src + c + 64), e = ld_nc(src + c + 96);
-    dst[c] = a;
-    dst[c + 32] = b2;
-    dst[c + 64] = d;
-    dst[c + 96] = e;
-  }
-  for (; c < n16; c += 32) dst[c] = ld_nc(src + c);
-}
-
+// One CTA moves one recompute row at a time: the K row, the V row and (optionally) the query
+// row form one list of 16-byte vectors; each thread loads up to kMaxVecPerThread of them
+// before storing any, so a whole row is in flight at once.
 __global__ void __launch_bounds__(kThreads) kv_scatter_kernel(
     int32_t L, int32_t kv_row16, int32_t q_row16, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new, int32_t src_by_position,
     const int32_t* __restrict__ idx, const int32_t* __restrict__ R, const uint4* __restrict__ q_src,
     uint4* __restrict__ q_dst, int32_t* __restrict__ dev_err) {
   const int b = blockIdx.y;
-  const int lane = threadIdx.x & 31;
+  pdl_wait();  // idx / R and the fresh rows may come from the previous kernels in the stream
+  pdl_launch_dependents();
   const int Rb = __ldg(R + b);
   if (Rb < 0 || Rb > L) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report_error(dev_err, EC_DEVERR_BAD_R);
     return;
   }
   const int64_t rowL = static_cast<int64_t>(b) * L;
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  const int nw = gridDim.x * kWarps;
-  for (int r = gw; r < Rb; r += nw) {
+  const int nq = q_dst != nullptr ? q_row16 : 0;
+  const int total = 2 * kv_row16 + nq;
+  for (int r = blockIdx.x; r < Rb; r += gridDim.x) {
     const int pos = __ldg(idx + rowL + r);
     if (pos < 0 || pos >= L) {
-      if (lane == 0) report_error(dev_err, EC_DEVERR_BAD_IDX);
+      if (threadIdx.x == 0) report_error(dev_err, EC_DEVERR_BAD_IDX);
       continue;
     }
     const int src = src_by_position ? pos : r;
-    const int64_t dst_off = (rowL + pos) * kv_row16;
-    const int64_t src_off = (rowL + src) * kv_row16;
-    warp_copy(k_cache + dst_off, k_new + src_off, kv_row16, lane);
-    warp_copy(v_cache + dst_off, v_new + src_off, kv_row16, lane);
-    if (q_dst != nullptr) warp_copy(q_dst + (rowL + r) * q_row16, q_src + (rowL + pos) * q_row16, q_row16, lane);
+    const int64_t dst_kv = (rowL + pos) * kv_row16;
+    const int64_t src_kv = (rowL + src) * kv_row16;
+    const int64_t dst_q = (rowL + r) * q_row16;
+    const int64_t src_q = (rowL + pos) * q_row16;
+    for (int base = 0; base < total; base += kThreads * kMaxVecPerThread) {
+      uint4 v[kMaxVecPerThread];
+#pragma unroll
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int e = base + threadIdx.x + u * kThreads;
+        if (e < kv_row16) v[u] = ld_nc(k_new + src_kv + e);
+        else if (e < 2 * kv_row16) v[u] = ld_nc(v_new + src_kv + (e - kv_row16));
+        else if (e < total) v[u] = ld_nc(q_src + src_q + (e - 2 * kv_row16));
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int e = base + threadIdx.x + u * kThreads;
+        if (e < kv_row16) k_cache[dst_kv + e] = v[u];
+        else if (e < 2 * kv_row16) v_cache[dst_kv + (e - kv_row16)] = v[u];
+        else if (e < total) q_dst[dst_q + (e - 2 * kv_row16)] = v[u];
+      }
+    }
   }
 }
 
@@ -79,16 +86,15 @@ cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, 
                               cudaStream_t s) {
   const int32_t kv_row16 = p.Hkv * p.D * 2 / 16;
   const int32_t q_row16 = p.Hq * p.D * 2 / 16;
-  const int64_t want = (static_cast<int64_t>(p.L) + kWarps - 1) / kWarps;
-  const int64_t cap = std::max<int64_t>(1, 2432 / (static_cast<int64_t>(p.B) * kWarps));
-  const int gx = static_cast<int>(std::max<int64_t>(1, std::min(want, cap)));
+  // one CTA per recompute row, at most ~8 per SM in total; R lives on the device, so the
+  // grid is sized for R = L and CTAs stride over the rows
+  const int64_t cap = std::max<int64_t>(1, 1216 / static_cast<int64_t>(p.B));
+  const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.L, cap)));
   const dim3 grid(gx, p.B);
-  kv_scatter_kernel<<<grid, kThreads, 0, s>>>(p.L, kv_row16, q_row16, static_cast<uint4*>(k_cache),
-                                              static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
-                                              static_cast<const uint4*>(v_new), src_by_position, idx, R,
-                                              static_cast<const uint4*>(q_src), static_cast<uint4*>(q_dst),
-                                              dev_err);
-  return cudaGetLastError();
+  return launch_pdl(kv_scatter_kernel, grid, dim3(kThreads), 0, s, p.L, kv_row16, q_row16,
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
+                    static_cast<const uint4*>(v_new), src_by_position, idx, R, static_cast<const uint4*>(q_src),
+                    static_cast<uint4*>(q_dst), dev_err);
 }
 
 }  // namespace ec

@@ -7,9 +7,10 @@
 // full one, otherwise it recomputes the current masked tokens plus the k most recently
 // decoded tokens, taken from a decode history; §2.3: the history costs O(k) memory.
 //
-// One CTA per sequence. Candidates live in shared memory (C_max <= 1024); the commit set is
-// found by ranking (O(C^2) comparisons, tiny for the block sizes in use). The recompute set
-// is built as an L-bit bitmap in shared memory (mask bits OR the last-k history bits) and
+// One CTA per sequence. The mask row becomes an L-bit bitmap in shared memory, the
+// candidates (C_max <= 1024) and the history (k <= 4096) are staged there too, all in one read
+// phase. The commit set is found by ranking (O(C^2) comparisons, tiny for the block sizes in
+// use); the committed bits are cleared, the last-k history bits set, and the bitmap is
 // compacted in ascending order with a block-wide prefix sum over the words' popcounts.
 #include <cmath>
 
@@ -23,16 +24,17 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCand = 1024;
 constexpr int kPerThread = kMaxCand / kThreads;  // candidates handled per thread
+constexpr int kMaxRingSmem = 4096;               // histories up to this length live in smem
 
 struct SelShared {
   int pos[kMaxCand];
   float conf[kMaxCand];
   unsigned char valid[kMaxCand];
   unsigned char chosen[kMaxCand];
+  int ring[kMaxRingSmem];
   int warp_tmp[kWarps];
   float warp_e[kWarps];
   int warp_nan[kWarps];
-  int n_dec_eff;
   int head;
   int count;
   int full;
@@ -80,6 +82,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, SelShared
   return before + incl - v;
 }
 
+__device__ __forceinline__ bool bit_set(const uint32_t* bm, int p) { return (bm[p >> 5] >> (p & 31)) & 1u; }
+
+// One CTA per sequence. All global reads are issued in one phase (mask bitmap, candidates,
+// history); the decisions then run on shared memory; global writes are fire-and-forget.
 __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     int32_t L, int32_t C_max, int32_t k, int32_t n_dec, float tau, const int32_t* __restrict__ cand_pos,
     const int32_t* __restrict__ cand_count, const int32_t* __restrict__ ids, const float* __restrict__ entropy,
@@ -87,13 +93,20 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     int32_t* __restrict__ ring, int32_t* __restrict__ ring_head, int32_t* __restrict__ ring_count,
     int32_t* __restrict__ dec_pos, float* __restrict__ E_out, uint8_t* __restrict__ flag_out,
     int32_t* __restrict__ idx, int32_t* __restrict__ R_out, int32_t* __restrict__ dev_err) {
-  extern __shared__ uint32_t bitmap[];  // ceil(L / 32) words
+  extern __shared__ uint32_t bitmap[];  // ceil(L / 32) words: the recompute set under construction
   __shared__ SelShared sh;
   const int b = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t rowL = static_cast<int64_t>(b) * L;
   const int64_t rowC = static_cast<int64_t>(b) * C_max;
+  int32_t* const ring_g = ring + static_cast<int64_t>(b) * k;
+  const bool ring_in_smem = k <= kMaxRingSmem;
+  int* const rs = ring_in_smem ? sh.ring : ring_g;
 
+  pdl_wait();  // decode results and state may come from the previous kernels in the stream
+  pdl_launch_dependents();
+
+  // ---- phase A: every global read ----------------------------------------------------------
   if (tid == 0) {
     int h = ring_head[b], c = ring_count[b];
     if (h < 0 || h >= k || c < 0 || c > k) {
@@ -103,62 +116,51 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     }
     sh.head = h;
     sh.count = c;
+    sh.carry = 0;
   }
   int count = __ldg(cand_count + b);
   if (count < 0 || count > C_max) {
     if (tid == 0) report_error(dev_err, EC_DEVERR_BAD_R);
     count = min(max(count, 0), C_max);
   }
-
-  // 1. Load candidates; a position outside [0, L) or not masked is invalid.
+  for (int p0 = warp << 5; p0 < L; p0 += kThreads) {  // mask -> bitmap, one warp per 32 positions
+    const int p = p0 + lane;
+    const bool m = p < L && mask[rowL + p] != 0;
+    const uint32_t bits = __ballot_sync(0xffffffffu, m);
+    if (lane == 0) bitmap[p0 >> 5] = bits;
+  }
+  if (ring_in_smem)
+    for (int t = tid; t < k; t += kThreads) sh.ring[t] = ring_g[t];
 #pragma unroll
   for (int q = 0; q < kPerThread; ++q) {
     const int i = tid + q * kThreads;
     if (i < count) {
       const int p = __ldg(cand_pos + rowC + i);
-      const bool in_range = p >= 0 && p < L;
-      const bool ok = in_range && mask[rowL + p] != 0;
       float c = __ldg(log_conf + rowC + i);
       if (isnan(c)) c = -INFINITY;  // NaN confidence ranks lowest
-      sh.pos[i] = in_range ? p : -1;
+      sh.pos[i] = (p >= 0 && p < L) ? p : -1;
       sh.conf[i] = c;
-      sh.valid[i] = ok ? 1 : 0;
-      if (!ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
     }
   }
   __syncthreads();
-  // A position listed twice keeps only its first occurrence.
-  unsigned char dup[kPerThread];
-#pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
-    const int i = tid + q * kThreads;
-    dup[q] = 0;
-    if (i < count && sh.valid[i]) {
-      for (int j = 0; j < i; ++j)
-        if (sh.valid[j] && sh.pos[j] == sh.pos[i]) {
-          dup[q] = 1;
-          break;
-        }
-    }
-  }
-  __syncthreads();
+
+  // ---- phase B: validity (in range, masked, first occurrence) and the committed set D ------
   int nvalid_local = 0;
 #pragma unroll
   for (int q = 0; q < kPerThread; ++q) {
     const int i = tid + q * kThreads;
     if (i < count) {
-      if (dup[q]) {
-        sh.valid[i] = 0;
-        report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
-      }
-      nvalid_local += sh.valid[i];
+      const int p = sh.pos[i];
+      bool ok = p >= 0 && bit_set(bitmap, p);
+      for (int j = 0; ok && j < i; ++j)
+        if (sh.pos[j] == p) ok = false;  // a position listed twice keeps its first occurrence
+      if (!ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
+      sh.valid[i] = ok ? 1 : 0;
+      nvalid_local += ok ? 1 : 0;
     }
   }
-  __syncthreads();
-  const int nvalid = block_sum_int(nvalid_local, sh);
+  const int nvalid = block_sum_int(nvalid_local, sh);  // contains __syncthreads
   const int nD = min(n_dec, nvalid);
-
-  // 2. D = the nD best-ranked valid candidates.
 #pragma unroll
   for (int q = 0; q < kPerThread; ++q) {
     const int i = tid + q * kThreads;
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
   }
   __syncthreads();
 
-  // 3. Commit, record dec_pos in ascending position order, push onto the ring, reduce E.
+  // ---- phase C: commit, dec_pos, history push, E = max entropy over D -----------------------
   const int head0 = sh.head;
   float emax = -INFINITY;
   int any_nan = 0;
@@ -189,25 +191,27 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
         if (sh.chosen[j] && sh.pos[j] < p) ++ord;
       tokens[rowL + p] = __ldg(ids + rowC + i);
       mask[rowL + p] = 0;
+      atomicAnd(&bitmap[p >> 5], ~(1u << (p & 31)));
       dec_pos[static_cast<int64_t>(b) * n_dec + ord] = p;
-      if (ord >= nD - k) ring[static_cast<int64_t>(b) * k + (head0 + ord) % k] = p;
+      if (ord >= nD - k) {  // only the last k of D survive in the history
+        const int slot = (head0 + ord) % k;
+        rs[slot] = p;
+        if (ring_in_smem) ring_g[slot] = p;
+      }
       const float h = __ldg(entropy + rowC + i);
       if (isnan(h)) any_nan = 1;
       else emax = fmaxf(emax, h);
     }
   }
   for (int t = nD + tid; t < n_dec; t += kThreads) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
-  {
-    const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
-      any_nan |= __shfl_xor_sync(0xffffffffu, any_nan, off);
-    }
-    if (lane == 0) {
-      sh.warp_e[warp] = emax;
-      sh.warp_nan[warp] = any_nan;
-    }
+  for (int off = 16; off > 0; off >>= 1) {
+    emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
+    any_nan |= __shfl_xor_sync(0xffffffffu, any_nan, off);
+  }
+  if (lane == 0) {
+    sh.warp_e[warp] = emax;
+    sh.warp_nan[warp] = any_nan;
   }
   __syncthreads();
   if (tid == 0) {
@@ -238,30 +242,19 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     sh.head = head1;
     sh.count = count1;
     sh.full = full;
-    sh.carry = 0;
   }
-  __syncthreads();  // commits, ring writes and the new head/count are visible to the block
+  __syncthreads();
 
-  // 4. Recompute set.
+  // ---- phase D: the recompute set ------------------------------------------------------------
   if (sh.full) {
     for (int r = tid; r < L; r += kThreads) idx[rowL + r] = r;
     if (tid == 0) R_out[b] = L;
     return;
   }
   const int nwords = (L + 31) >> 5;
-  {
-    const int lane = tid & 31, warp = tid >> 5;
-    for (int p0 = warp << 5; p0 < L; p0 += kThreads) {  // one warp per 32 positions
-      const int p = p0 + lane;
-      const bool m = p < L && mask[rowL + p] != 0;
-      const uint32_t bits = __ballot_sync(0xffffffffu, m);
-      if (lane == 0) bitmap[p0 >> 5] = bits;
-    }
-  }
-  __syncthreads();
   const int head1 = sh.head, count1 = sh.count;
-  for (int t = tid; t < count1; t += kThreads) {
-    const int p = ring[static_cast<int64_t>(b) * k + ((head1 - 1 - t) % k + k) % k];
+  for (int t = tid; t < count1; t += kThreads) {  // the last min(k, count) decoded positions
+    const int p = rs[((head1 - 1 - t) % k + k) % k];
     if (p >= 0 && p < L) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
     else report_error(dev_err, EC_DEVERR_BAD_IDX);
   }
@@ -298,10 +291,9 @@ cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, cons
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  select_recompute_kernel<<<p.B, kThreads, smem, s>>>(
-      p.L, p.C_max, p.k, p.n_dec, p.tau, cand_pos, cand_count, ids, entropy, log_conf, st.tokens, st.mask, st.ring,
-      st.ring_head, st.ring_count, st.dec_pos, st.E, st.flag, st.idx, st.R, st.dev_err);
-  return cudaGetLastError();
+  return launch_pdl(select_recompute_kernel, dim3(p.B), dim3(kThreads), smem, s, p.L, p.C_max, p.k, p.n_dec, p.tau,
+                    cand_pos, cand_count, ids, entropy, log_conf, st.tokens, st.mask, st.ring, st.ring_head,
+                    st.ring_count, st.dec_pos, st.E, st.flag, st.idx, st.R, st.dev_err);
 }
 
 }  // namespace ec

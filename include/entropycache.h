@@ -206,9 +206,8 @@ ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const 
  *         of out are not written); k_cache, v_cache bf16 [B, L, Hkv, D].
  * R       int32 [B] on the device (read by the kernel: no host synchronisation).
  * scale   softmax scale, normally 1/sqrt(D).
- * ws      at least ec_partial_attention_workspace_size(p) bytes, zero-filled before its
- *         first use; the library returns its counters to zero. Calls sharing a workspace
- *         must not overlap in time.
+ * ws      at least ec_partial_attention_workspace_size(p) bytes (reserved: the key-split
+ *         merge runs in on-chip shared memory of a 4-CTA cluster).
  * Products run on bf16 tensor cores with fp32 accumulation; probabilities are rounded to
  * bf16 before the PV product. A pipeline wait that exceeds its limit sets
  * EC_DEVERR_TIMEOUT in dev_err (if given) and leaves that tile unwritten. */

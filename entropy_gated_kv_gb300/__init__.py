@@ -30,6 +30,7 @@ __all__ = [
     "workspace",
     "entropy_decode",
     "entropy_decode_workspace_size",
+    "entropy_decode_noalloc",
     "select_recompute",
     "kv_scatter",
     "partial_attention",
@@ -149,6 +150,24 @@ def entropy_decode(logits: torch.Tensor, V: int | None = None, ws: torch.Tensor 
     st = lib().ec_entropy_decode(_vp(logits), logits.stride(0), n, V, code, _vp(out[0]), _vp(out[1]), _vp(out[2]),
                                  _vp(ws), ws.numel(), _stream(stream))
     C.check(st, "ec_entropy_decode")
+    return out
+
+
+def entropy_decode_noalloc(logits: torch.Tensor, V: int | None = None, out: tuple | None = None, stream=None):
+    """(a) like entropy_decode, but with no workspace: for callers that cannot allocate device
+    memory. The scratch is a 1 MiB array owned by the library; calls that overlap on the GPU
+    race, and the first call on a device must come before any stream capture."""
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [n_rows, row_stride] with unit inner stride")
+    n, V = logits.shape[0], (V if V is not None else logits.shape[1])
+    code = _dtype_code(logits.dtype)
+    if out is None:
+        out = (torch.empty(n, dtype=torch.int32, device=logits.device),
+               torch.empty(n, dtype=torch.float32, device=logits.device),
+               torch.empty(n, dtype=torch.float32, device=logits.device))
+    st = lib().ec_entropy_decode_noalloc(_vp(logits), logits.stride(0), n, V, code, _vp(out[0]), _vp(out[1]),
+                                         _vp(out[2]), _stream(stream))
+    C.check(st, "ec_entropy_decode_noalloc")
     return out
 
 

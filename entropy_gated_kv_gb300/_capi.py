@@ -24,6 +24,8 @@ EC_DEVERR_TIMEOUT = 0x8
 EC_F32 = 0
 EC_BF16 = 1
 
+EC_NOALLOC_SCRATCH_BYTES = 1 << 20
+
 _p = ctypes.c_void_p
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
@@ -52,6 +54,7 @@ SIGNATURES: dict[str, tuple] = {
     "ec_read_device_error": (_i32, [_p, ctypes.POINTER(_i32), _p]),
     "ec_entropy_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
     "ec_entropy_decode": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
+    "ec_entropy_decode_noalloc": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p]),
     "ec_select_recompute": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _p, _p, _p]),
     "ec_kv_scatter": (_i32, [ctypes.POINTER(EcParams), _p, _p, _p, _p, _i32, _p, _p, _p, _p]),
     "ec_partial_attention_workspace_size": (_sz, [ctypes.POINTER(EcParams)]),

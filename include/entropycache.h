@@ -152,6 +152,29 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
                             int32_t dtype, int32_t* ids, float* entropy, float* log_conf,
                             void* ws, size_t ws_bytes, ec_stream_t stream);
 
+/* ---- (a) without a workspace, for callers that cannot allocate -------------------------
+ * The paper has no counterpart to this entry point: it is a deployment convenience.
+ * Same computation, arguments and results as ec_entropy_decode, minus the workspace. It is
+ * for callers that hold only their input and output buffers and cannot allocate device
+ * memory: a plugin or custom-op interface of a serving runtime that passes an op its tensors
+ * but no allocator, or latency-critical code that must not call cudaMalloc because it
+ * synchronises the whole device.
+ * Scratch lives in a library-owned static device array of EC_NOALLOC_SCRATCH_BYTES (1 MiB)
+ * that every GPU which loads the library holds until the process exits. A request that
+ * needs more (ec_entropy_decode_workspace_size(n_rows, V, dtype) > EC_NOALLOC_SCRATCH_BYTES,
+ * e.g. more than about 4000 rows of a 126464-entry bf16 vocabulary) returns
+ * EC_ERR_UNSUPPORTED and launches nothing.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current): make that first call before any stream capture.
+ * Every call shares the one array, which keeps the last call's contents; each call clears the
+ * counters it needs with an asynchronous memset on `stream` before its kernel. Calls whose
+ * executions overlap on the GPU (other streams, other host threads) race and give wrong
+ * results: order them. No cudaMalloc, cudaFree or allocating library routine is called. */
+#define EC_NOALLOC_SCRATCH_BYTES (1u << 20)
+ec_status ec_entropy_decode_noalloc(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
+                                    int32_t dtype, int32_t* ids, float* entropy, float* log_conf,
+                                    ec_stream_t stream);
+
 /* ---- (b)+(c) commit, max-entropy gate, decode history, recompute set -------------------
  * Follows the skip decision and selection stage of the workflow (zh summary §2.2: full
  * recompute iff E_{t+1} = max over newly decoded tokens of their entropy exceeds tau,

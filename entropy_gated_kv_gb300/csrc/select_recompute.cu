@@ -29,6 +29,8 @@ constexpr int kMaxRingSmem = 4096;               // histories up to this length 
 struct SelShared {
   int pos[kMaxCand];
   float conf[kMaxCand];
+  float ent[kMaxCand];
+  int id[kMaxCand];
   unsigned char valid[kMaxCand];
   unsigned char chosen[kMaxCand];
   int ring[kMaxRingSmem];
@@ -39,6 +41,7 @@ struct SelShared {
   int count;
   int full;
   int carry;
+  int nd;
 };
 
 // Candidate j outranks candidate i: higher confidence; equal confidence, smaller position.
@@ -132,78 +135,124 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
   if (ring_in_smem)
     for (int t = tid; t < k; t += kThreads) sh.ring[t] = ring_g[t];
 #pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
+  for (int q = 0; q < kPerThread; ++q) {  // every field of every candidate row, in one round trip
     const int i = tid + q * kThreads;
-    if (i < count) {
+    if (i < C_max) {
       const int p = __ldg(cand_pos + rowC + i);
       float c = __ldg(log_conf + rowC + i);
       if (isnan(c)) c = -INFINITY;  // NaN confidence ranks lowest
       sh.pos[i] = (p >= 0 && p < L) ? p : -1;
       sh.conf[i] = c;
+      sh.ent[i] = __ldg(entropy + rowC + i);
+      sh.id[i] = __ldg(ids + rowC + i);
     }
   }
   __syncthreads();
 
-  // ---- phase B: validity (in range, masked, first occurrence) and the committed set D ------
-  int nvalid_local = 0;
-#pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
-    const int i = tid + q * kThreads;
-    if (i < count) {
-      const int p = sh.pos[i];
-      bool ok = p >= 0 && bit_set(bitmap, p);
-      for (int j = 0; ok && j < i; ++j)
-        if (sh.pos[j] == p) ok = false;  // a position listed twice keeps its first occurrence
-      if (!ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
-      sh.valid[i] = ok ? 1 : 0;
-      nvalid_local += ok ? 1 : 0;
-    }
-  }
-  const int nvalid = block_sum_int(nvalid_local, sh);  // contains __syncthreads
-  const int nD = min(n_dec, nvalid);
-#pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
-    const int i = tid + q * kThreads;
-    if (i < count) {
-      int rank = 0;
-      if (sh.valid[i]) {
-        const float ci = sh.conf[i];
-        const int pi = sh.pos[i];
-        for (int j = 0; j < count; ++j)
-          if (j != i && sh.valid[j] && outranks(sh.conf[j], sh.pos[j], ci, pi)) ++rank;
-      }
-      sh.chosen[i] = (sh.valid[i] && rank < nD) ? 1 : 0;
-    }
-  }
-  __syncthreads();
-
-  // ---- phase C: commit, dec_pos, history push, E = max entropy over D -----------------------
+  // ---- phases B + C: validity, the committed set D, commit, history push, E ---------------
+  // B: a candidate is valid if in range, still masked and the first listing of its position;
+  //    D = the nD = min(n_dec, #valid) best-ranked valid candidates.
+  // C: commit D, record dec_pos in ascending position order, push D onto the ring, reduce E.
   const int head0 = sh.head;
+  int nD = 0;
   float emax = -INFINITY;
   int any_nan = 0;
+  if (C_max <= 32) {
+    // One warp holds every candidate: ranking by shuffles, no shared-memory loops.
+    if (warp == 0) {
+      const bool in = lane < count;
+      const int p = in ? sh.pos[lane] : -1;
+      const float c = in ? sh.conf[lane] : -INFINITY;
+      bool ok = in && p >= 0 && bit_set(bitmap, p);
+      const unsigned same = __match_any_sync(0xffffffffu, ok ? p : -2 - lane);
+      ok = ok && (__ffs(same) - 1 == lane);  // first listing of its position
+      if (in && !ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
+      const unsigned vmask = __ballot_sync(0xffffffffu, ok);
+      nD = min(n_dec, __popc(vmask));
+      int rank = 0;
 #pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
-    const int i = tid + q * kThreads;
-    if (i < count && sh.chosen[i]) {
-      const int p = sh.pos[i];
-      int ord = 0;
-      for (int j = 0; j < count; ++j)
-        if (sh.chosen[j] && sh.pos[j] < p) ++ord;
-      tokens[rowL + p] = __ldg(ids + rowC + i);
-      mask[rowL + p] = 0;
-      atomicAnd(&bitmap[p >> 5], ~(1u << (p & 31)));
-      dec_pos[static_cast<int64_t>(b) * n_dec + ord] = p;
-      if (ord >= nD - k) {  // only the last k of D survive in the history
-        const int slot = (head0 + ord) % k;
-        rs[slot] = p;
-        if (ring_in_smem) ring_g[slot] = p;
+      for (int j = 0; j < 32; ++j) {
+        const float cj = __shfl_sync(0xffffffffu, c, j);
+        const int pj = __shfl_sync(0xffffffffu, p, j);
+        if (((vmask >> j) & 1u) && j != lane && outranks(cj, pj, c, p)) ++rank;
       }
-      const float h = __ldg(entropy + rowC + i);
-      if (isnan(h)) any_nan = 1;
-      else emax = fmaxf(emax, h);
+      const bool chosen = ok && rank < nD;
+      const unsigned cmask = __ballot_sync(0xffffffffu, chosen);
+      int ord = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int pj = __shfl_sync(0xffffffffu, p, j);
+        if (((cmask >> j) & 1u) && pj < p) ++ord;
+      }
+      if (chosen) {
+        tokens[rowL + p] = sh.id[lane];
+        mask[rowL + p] = 0;
+        atomicAnd(&bitmap[p >> 5], ~(1u << (p & 31)));
+        dec_pos[static_cast<int64_t>(b) * n_dec + ord] = p;
+        if (ord >= nD - k) {  // only the last k of D survive in the history
+          const int slot = (head0 + ord) % k;
+          rs[slot] = p;
+          if (ring_in_smem) ring_g[slot] = p;
+        }
+        const float h = sh.ent[lane];
+        if (isnan(h)) any_nan = 1;
+        else emax = fmaxf(emax, h);
+      }
+    }
+  } else {
+    int nvalid_local = 0;
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < count) {
+        const int p = sh.pos[i];
+        bool ok = p >= 0 && bit_set(bitmap, p);
+        for (int j = 0; ok && j < i; ++j)
+          if (sh.pos[j] == p) ok = false;  // a position listed twice keeps its first occurrence
+        if (!ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
+        sh.valid[i] = ok ? 1 : 0;
+        nvalid_local += ok ? 1 : 0;
+      }
+    }
+    nD = min(n_dec, block_sum_int(nvalid_local, sh));  // contains __syncthreads
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < count) {
+        int rank = 0;
+        if (sh.valid[i]) {
+          const float ci = sh.conf[i];
+          const int pi = sh.pos[i];
+          for (int j = 0; j < count; ++j)
+            if (j != i && sh.valid[j] && outranks(sh.conf[j], sh.pos[j], ci, pi)) ++rank;
+        }
+        sh.chosen[i] = (sh.valid[i] && rank < nD) ? 1 : 0;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kPerThread; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < count && sh.chosen[i]) {
+        const int p = sh.pos[i];
+        int ord = 0;
+        for (int j = 0; j < count; ++j)
+          if (sh.chosen[j] && sh.pos[j] < p) ++ord;
+        tokens[rowL + p] = sh.id[i];
+        mask[rowL + p] = 0;
+        atomicAnd(&bitmap[p >> 5], ~(1u << (p & 31)));
+        dec_pos[static_cast<int64_t>(b) * n_dec + ord] = p;
+        if (ord >= nD - k) {  // only the last k of D survive in the history
+          const int slot = (head0 + ord) % k;
+          rs[slot] = p;
+          if (ring_in_smem) ring_g[slot] = p;
+        }
+        const float h = sh.ent[i];
+        if (isnan(h)) any_nan = 1;
+        else emax = fmaxf(emax, h);
+      }
     }
   }
-  for (int t = nD + tid; t < n_dec; t += kThreads) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
@@ -213,8 +262,10 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     sh.warp_e[warp] = emax;
     sh.warp_nan[warp] = any_nan;
   }
+  if (tid == 0) sh.nd = nD;  // thread 0 is in warp 0, which knows nD on both paths
   __syncthreads();
   if (tid == 0) {
+    const int nd = sh.nd;
     float e = -INFINITY;
     int nan_seen = 0;
     for (int w = 0; w < kWarps; ++w) {
@@ -223,7 +274,7 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     }
     float E;
     int full;
-    if (nD == 0) {
+    if (nd == 0) {
       E = 0.f;  // nothing decoded: E = 0
       full = (E > tau) ? 1 : 0;
     } else if (nan_seen) {
@@ -235,15 +286,17 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     }
     E_out[b] = E;
     flag_out[b] = static_cast<uint8_t>(full);
-    const int head1 = (head0 + nD) % k;
-    const int count1 = min(sh.count + nD, k);
+    const int head1 = (head0 + nd) % k;
+    const int count1 = min(sh.count + nd, k);
     ring_head[b] = head1;
     ring_count[b] = count1;
     sh.head = head1;
     sh.count = count1;
     sh.full = full;
+    sh.carry = 0;
   }
   __syncthreads();
+  for (int t = sh.nd + tid; t < n_dec; t += kThreads) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
 
   // ---- phase D: the recompute set ------------------------------------------------------------
   if (sh.full) {

@@ -24,7 +24,10 @@ Logit distributions:
                logit = -1.1 ln rho + N(0, 1)
   trace        per (step, sequence) a Bernoulli(0.1) draw (step 0 always high) picks
                high: every row N(0, 0.5^2)  (entropy about ln V)
-               low:  every row N(0, 1) plus 20 at one seeded token (entropy about 0.005)
+               low:  every row N(0, 1) plus a peak at one seeded token; with c candidate
+                     rows this step (c = 32 - step mod 32), row i's peak is
+                     17.25 - 0.25 (c - 1 - i), so the most confident row has entropy about 0.05
+                     and the confidences of the best rows lie ~1e-3 apart
 K/V cache, queries ~ N(0, 1); fresh K/V rows = cache + N(0, 0.05^2); all bf16.
 """
 from __future__ import annotations
@@ -41,6 +44,7 @@ __all__ = [
     "rng_for",
     "snapshot_state",
     "step_logits",
+    "layer_pool",
     "layer_tensors",
     "trace_candidates",
 ]
@@ -217,7 +221,9 @@ def step_logits(w: Workload, step: int = 0) -> np.ndarray:
             else:
                 out[b] = r.standard_normal((C, V), dtype=np.float32)
                 peak = r.integers(0, V, size=C)
-                out[b, np.arange(C), peak] += np.float32(20.0)
+                c = w.block - step % w.block
+                height = 17.25 - 0.25 * (c - 1 - np.arange(C))
+                out[b, np.arange(C), peak] += height.astype(np.float32)
         else:
             raise ValueError(w.logits_kind)
     return _finish_logits(w, out)
@@ -231,30 +237,35 @@ def _normal_bf16(r: np.random.Generator, shape: tuple[int, ...]) -> np.ndarray:
     return to_bf16_bits(r.standard_normal(shape, dtype=np.float32))
 
 
-def layer_tensors(w: Workload, layer: int = 0) -> dict:
-    """bf16 bit patterns for one layer: k_cache, v_cache, k_src, v_src [B, L, Hkv, D] and
-    q_src [B, L, Hq, D]. Fresh rows k_src/v_src = cache + N(0, 0.05^2).
-
-    Multi-layer workloads draw one pool per tensor and give layer l a seeded circular shift
-    of it, so 32 layers cost one draw.
-    """
+def layer_pool(w: Workload) -> dict:
+    """One draw of every per-layer tensor (bf16 bit patterns): k_cache, v_cache, k_src, v_src
+    [B, L, Hkv, D] and q_src [B, L, Hq, D]; fresh rows k_src/v_src = cache + N(0, 0.05^2)."""
     B, L, Hq, Hkv, D = w.B, w.L, w.Hq, w.Hkv, w.D
     kv_shape = (B, L, Hkv, D)
     q_shape = (B, L, Hq, D)
-    base = layer if w.n_layers == 1 else 0
     out = {}
     for j, name in enumerate(("k_cache", "v_cache")):
-        cache = _normal_bf16(rng_for(w.seed, 40, base, j), kv_shape)
-        noise = rng_for(w.seed, 41, base, j).standard_normal(kv_shape, dtype=np.float32)
+        cache = _normal_bf16(rng_for(w.seed, 40, 0, j), kv_shape)
+        noise = rng_for(w.seed, 41, 0, j).standard_normal(kv_shape, dtype=np.float32)
         noise *= np.float32(0.05)
         noise += bf16_bits_to_f32(cache)
         out[name] = cache
         out[name.replace("cache", "src")] = to_bf16_bits(noise)
         del noise
-    out["q_src"] = _normal_bf16(rng_for(w.seed, 42, base), q_shape)
-    if w.n_layers > 1 and layer > 0:
-        shift = int(rng_for(w.seed, 43, layer).integers(1, 1 << 30))
-        for name in list(out):
-            flat = out[name].reshape(-1)
-            out[name] = np.roll(flat, shift % flat.size).reshape(out[name].shape)
+    out["q_src"] = _normal_bf16(rng_for(w.seed, 42, 0), q_shape)
+    return out
+
+
+def layer_tensors(w: Workload, layer: int = 0, pool: dict | None = None) -> dict:
+    """bf16 bit patterns for one layer (see layer_pool). Layer 0 is the pool itself; layer l > 0
+    of a multi-layer workload is a seeded circular shift of the pool, so 32 layers cost one
+    draw. Pass `pool` to reuse a draw across calls."""
+    base = pool if pool is not None else layer_pool(w)
+    if w.n_layers == 1 or layer == 0:
+        return dict(base)
+    shift = int(rng_for(w.seed, 43, layer).integers(1, 1 << 30))
+    out = {}
+    for name, a in base.items():
+        flat = a.reshape(-1)
+        out[name] = np.roll(flat, shift % flat.size).reshape(a.shape)
     return out

@@ -46,6 +46,57 @@ NCOPY = 4
 CHUNK = 500
 
 
+def kernel_source_hash(name: str) -> str:
+    """Hash of a kernel's source file (ncu counters are only valid for the source they came from)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "entropy_gated_kv_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, source: str) -> float | None:
+    """DRAM bytes per launch from profiles/traffic.json, if captured on the current source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)[kernel]
+        return float(d["dram_bytes_per_launch"]) if d["source_sha"] == kernel_source_hash(source) else None
+    except Exception:
+        return None
+
+
+def run_profile(steps: int) -> None:
+    """A few eager steps of the workload (no graphs, no timing): a short program for ncu."""
+    import torch
+
+    import entropy_gated_kv_gb300 as E
+    from entropy_gated_kv_gb300 import build as B
+
+    B.build()
+    w = W.workload(WORKLOAD)
+    p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
+                 logits_dtype=w.logits_dtype)
+    st_h = W.snapshot_state(w)
+    lay = W.layer_tensors(w, 0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    layer = {n: bf(lay[n]) for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
+    layer["out"] = torch.zeros(w.B, w.L, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
+    logits = bf(W.step_logits(w))
+    cp = torch.from_numpy(st_h["cand_pos"]).cuda()
+    cc = torch.from_numpy(st_h["cand_count"]).cuda()
+    ws = E.workspace(E.step_workspace_size(p))
+    for _ in range(steps):
+        st = E.DecodeState.from_arrays(p, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
+                                       ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
+        E.step(p, st, logits, cp, cc, [layer], ws=ws)
+    torch.cuda.synchronize()
+    status, word = E.read_device_error(st.dev_err)
+    print(json.dumps({"profile_steps": steps, "R": int(st.R[0]), "flag": int(st.flag[0]), "status": status}))
+
+
 def peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -387,7 +438,8 @@ def emit_ours(args, res, rank, world):
     roof = dict(cands[dom][1])
     roof["kernel"] = dom
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    src = {"entropy_decode": "entropy_decode.cu", "partial_attention": "attention.cu"}[dom]
+    roof["traffic"] = profiled_traffic(dom, src)
     roof["peak_source"] = pk["source"] + " (burst; kernel timed alone)"
     line = {
         "metric": METRIC,
@@ -535,7 +587,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps and exit (a short program for ncu)")
     args = ap.parse_args()
+    if args.profile_steps > 0:
+        run_profile(args.profile_steps)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", 0))

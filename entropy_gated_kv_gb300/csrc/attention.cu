@@ -228,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
   pdl_launch_dependents();
   const Plan pl = make_plan(R, B, L, Hkv, nr, nclusters);
   const bool split_mode = pl.splits > 1;
+  Item split_item{};  // the shared tile's item, kept by the softmax warps for the merge
+  split_item.nrows = -1;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -328,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       const int item = cta_item(n, pl, cluster, rank, nclusters);
       if (item < 0) break;
       const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      if (split_mode) split_item = I;
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nblk; ++j) {
@@ -493,7 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     if (warp >= 2) {
       const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->recv, 0, abort_flag, dev_err, kWaitLimitNs));
       if (got && cluster < pl.tiles) {
-        const Item I = decode_item(cluster * pl.splits, pl, R, B, L, Hkv, nr);
+        // the tile is shared by the cluster; CTAs without a split of their own decode it here
+        const Item I = split_item.nrows >= 0 ? split_item : decode_item(cluster * pl.splits, pl, R, B, L, Hkv, nr);
         constexpr int kCols = D / 4;  // four threads per row, kCols columns each
         const int t = threadIdx.x - 64;
         const int srow = t >> 2;  // row within this CTA's slice

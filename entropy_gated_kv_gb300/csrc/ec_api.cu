@@ -57,6 +57,7 @@ ec_status check_state(const ec_state* st) {
   if (!st->tokens || !st->mask || !st->ring || !st->ring_head || !st->ring_count || !st->dec_pos || !st->E ||
       !st->flag || !st->idx || !st->R)
     return EC_ERR_INVALID_ARG;
+  if (!aligned16(st->mask)) return EC_ERR_INVALID_ARG;  // the mask row is read with 16-byte loads
   return EC_OK;
 }
 

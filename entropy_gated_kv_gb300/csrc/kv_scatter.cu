@@ -86,9 +86,16 @@ cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, 
                               cudaStream_t s) {
   const int32_t kv_row16 = p.Hkv * p.D * 2 / 16;
   const int32_t q_row16 = p.Hq * p.D * 2 / 16;
-  // one CTA per recompute row, at most ~8 per SM in total; R lives on the device, so the
-  // grid is sized for R = L and CTAs stride over the rows
-  const int64_t cap = std::max<int64_t>(1, 1216 / static_cast<int64_t>(p.B));
+  // one CTA per recompute row, at most two per SM in total so the whole grid is resident at
+  // once (the next kernel can then launch early); R lives on the device, so CTAs stride over
+  // the rows
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+  }
+  const int64_t cap = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / p.B);
   const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.L, cap)));
   const dim3 grid(gx, p.B);
   return launch_pdl(kv_scatter_kernel, grid, dim3(kThreads), 0, s, p.L, kv_row16, q_row16,

@@ -12,6 +12,7 @@
 // phase. The commit set is found by ranking (O(C^2) comparisons, tiny for the block sizes in
 // use); the committed bits are cleared, the last-k history bits set, and the bitmap is
 // compacted in ascending order with a block-wide prefix sum over the words' popcounts.
+#include <climits>
 #include <cmath>
 
 #include "ec_common.cuh"
@@ -41,7 +42,6 @@ struct SelShared {
   int count;
   int full;
   int carry;
-  int nd;
 };
 
 // Candidate j outranks candidate i: higher confidence; equal confidence, smaller position.
@@ -87,8 +87,64 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, SelShared
 
 __device__ __forceinline__ bool bit_set(const uint32_t* bm, int p) { return (bm[p >> 5] >> (p & 31)) & 1u; }
 
-// One CTA per sequence. All global reads are issued in one phase (mask bitmap, candidates,
-// history); the decisions then run on shared memory; global writes are fire-and-forget.
+// 32 mask bytes -> one bitmap word (bit t set when byte t is non-zero).
+__device__ __forceinline__ uint32_t bytes_to_bits(uint4 lo, uint4 hi) {
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) bits |= (((w[q] >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << (4 * q + e);
+  return bits;
+}
+
+// Warp-wide: the set bits of words [0, nwords) written to idx in ascending order; returns
+// the count (nwords <= 32). Lane w computes the prefix count of word w; then, word by word,
+// lane j writes bit j — independent iterations, no lane loops over its own bits.
+__device__ __forceinline__ int warp_compact(const uint32_t* bitmap, int nwords, int32_t* idx_row, int lane) {
+  const uint32_t mine = lane < nwords ? bitmap[lane] : 0u;
+  const int c = __popc(mine);
+  int incl = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  const int excl = incl - c;
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll 8
+  for (int w = 0; w < nwords; ++w) {
+    const uint32_t word = __shfl_sync(0xffffffffu, mine, w);
+    const int base = __shfl_sync(0xffffffffu, excl, w);
+    if ((word >> lane) & 1u) idx_row[base + __popc(word & below)] = (w << 5) + lane;
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Warp argmax over (confidence, -position): the best-ranked lane among `live`, or -1.
+__device__ __forceinline__ int warp_best(float c, int p, bool live, int lane) {
+  float bc = live ? c : -INFINITY;
+  int bp = live ? p : INT_MAX;
+  int bl = live ? lane : 32;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float oc = __shfl_xor_sync(0xffffffffu, bc, off);
+    const int op = __shfl_xor_sync(0xffffffffu, bp, off);
+    const int ol = __shfl_xor_sync(0xffffffffu, bl, off);
+    if (ol < 32 && (bl == 32 || outranks(oc, op, bc, bp))) {
+      bc = oc;
+      bp = op;
+      bl = ol;
+    }
+  }
+  return bl < 32 ? bl : -1;
+}
+
+// One CTA per sequence. One read phase stages the mask as an L-bit bitmap (16-byte loads),
+// the candidates and the history in shared memory. With at most 32 candidates a single warp
+// then ranks, commits, gates, pushes the history and edits the bitmap, and for L <= 1024 also
+// compacts it: two block barriers in all. Larger candidate lists and sequences use block-wide
+// loops.
 __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     int32_t L, int32_t C_max, int32_t k, int32_t n_dec, float tau, const int32_t* __restrict__ cand_pos,
     const int32_t* __restrict__ cand_count, const int32_t* __restrict__ ids, const float* __restrict__ entropy,
@@ -105,11 +161,13 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
   int32_t* const ring_g = ring + static_cast<int64_t>(b) * k;
   const bool ring_in_smem = k <= kMaxRingSmem;
   int* const rs = ring_in_smem ? sh.ring : ring_g;
+  const int nwords = (L + 31) >> 5;
+  const bool fast = C_max <= 32;
 
   pdl_wait();  // decode results and state may come from the previous kernels in the stream
   pdl_launch_dependents();
 
-  // ---- phase A: every global read ----------------------------------------------------------
+  // ---- phase A: every global read, one round trip ------------------------------------------
   if (tid == 0) {
     int h = ring_head[b], c = ring_count[b];
     if (h < 0 || h >= k || c < 0 || c > k) {
@@ -126,16 +184,25 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     if (tid == 0) report_error(dev_err, EC_DEVERR_BAD_R);
     count = min(max(count, 0), C_max);
   }
-  for (int p0 = warp << 5; p0 < L; p0 += kThreads) {  // mask -> bitmap, one warp per 32 positions
-    const int p = p0 + lane;
-    const bool m = p < L && mask[rowL + p] != 0;
-    const uint32_t bits = __ballot_sync(0xffffffffu, m);
-    if (lane == 0) bitmap[p0 >> 5] = bits;
+  if ((L & 15) == 0) {  // 16-byte aligned rows: two vector loads per 32 positions
+    const uint4* m4 = reinterpret_cast<const uint4*>(mask + rowL);
+    for (int w = tid; w < nwords; w += kThreads) {
+      const uint4 lo = m4[2 * w];
+      const uint4 hi = (32 * w + 16 < L) ? m4[2 * w + 1] : make_uint4(0, 0, 0, 0);
+      bitmap[w] = bytes_to_bits(lo, hi);
+    }
+  } else {
+    for (int p0 = warp << 5; p0 < L; p0 += kThreads) {  // one warp per 32 positions
+      const int p = p0 + lane;
+      const bool m = p < L && mask[rowL + p] != 0;
+      const uint32_t bits = __ballot_sync(0xffffffffu, m);
+      if (lane == 0) bitmap[p0 >> 5] = bits;
+    }
   }
   if (ring_in_smem)
     for (int t = tid; t < k; t += kThreads) sh.ring[t] = ring_g[t];
 #pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {  // every field of every candidate row, in one round trip
+  for (int q = 0; q < kPerThread; ++q) {  // every field of every candidate row
     const int i = tid + q * kThreads;
     if (i < C_max) {
       const int p = __ldg(cand_pos + rowC + i);
@@ -152,12 +219,10 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
   // ---- phases B + C: validity, the committed set D, commit, history push, E ---------------
   // B: a candidate is valid if in range, still masked and the first listing of its position;
   //    D = the nD = min(n_dec, #valid) best-ranked valid candidates.
-  // C: commit D, record dec_pos in ascending position order, push D onto the ring, reduce E.
+  // C: commit D, record dec_pos in ascending position order, push D onto the ring, reduce E,
+  //    gate, and mark the recompute set (clear D's mask bits, set the last-k history bits).
   const int head0 = sh.head;
-  int nD = 0;
-  float emax = -INFINITY;
-  int any_nan = 0;
-  if (C_max <= 32) {
+  if (fast) {
     // One warp holds every candidate: ranking by shuffles, no shared-memory loops.
     if (warp == 0) {
       const bool in = lane < count;
@@ -168,22 +233,24 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
       ok = ok && (__ffs(same) - 1 == lane);  // first listing of its position
       if (in && !ok) report_error(dev_err, EC_DEVERR_BAD_CAND_POS);
       const unsigned vmask = __ballot_sync(0xffffffffu, ok);
-      nD = min(n_dec, __popc(vmask));
-      int rank = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float cj = __shfl_sync(0xffffffffu, c, j);
-        const int pj = __shfl_sync(0xffffffffu, p, j);
-        if (((vmask >> j) & 1u) && j != lane && outranks(cj, pj, c, p)) ++rank;
+      const int nD = min(n_dec, __popc(vmask));
+      // D: nD rounds of a warp argmax over the not-yet-chosen valid candidates.
+      bool chosen = false;
+      for (int r = 0; r < nD; ++r) {
+        const int wl = warp_best(c, p, ok && !chosen, lane);
+        if (wl == lane) chosen = true;
       }
-      const bool chosen = ok && rank < nD;
       const unsigned cmask = __ballot_sync(0xffffffffu, chosen);
-      int ord = 0;
+      int ord = 0;  // rank of this position among D, ascending
+      if (nD > 1) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int pj = __shfl_sync(0xffffffffu, p, j);
-        if (((cmask >> j) & 1u) && pj < p) ++ord;
+        for (int j = 0; j < 32; ++j) {
+          const int pj = __shfl_sync(0xffffffffu, p, j);
+          if (((cmask >> j) & 1u) && pj < p) ++ord;
+        }
       }
+      float emax = -INFINITY;
+      int any_nan = 0;
       if (chosen) {
         tokens[rowL + p] = sh.id[lane];
         mask[rowL + p] = 0;
@@ -197,6 +264,36 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
         const float h = sh.ent[lane];
         if (isnan(h)) any_nan = 1;
         else emax = fmaxf(emax, h);
+      }
+      for (int t = nD + lane; t < n_dec; t += 32) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
+        any_nan |= __shfl_xor_sync(0xffffffffu, any_nan, off);
+      }
+      const float E = nD == 0 ? 0.f : (any_nan ? NAN : emax);  // nothing decoded: E = 0
+      const int full = (nD > 0 && any_nan) ? 1 : (E > tau ? 1 : 0);
+      const int head1 = (head0 + nD) % k;
+      const int count1 = min(sh.count + nD, k);
+      if (lane == 0) {
+        E_out[b] = E;
+        flag_out[b] = static_cast<uint8_t>(full);
+        ring_head[b] = head1;
+        ring_count[b] = count1;
+        sh.full = full;
+      }
+      __syncwarp();
+      if (!full) {
+        for (int t = lane; t < count1; t += 32) {  // the last min(k, count) decoded positions
+          const int q = rs[((head1 - 1 - t) % k + k) % k];
+          if (q >= 0 && q < L) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
+          else report_error(dev_err, EC_DEVERR_BAD_IDX);
+        }
+        __syncwarp();
+        if (nwords <= 32) {
+          const int R = warp_compact(bitmap, nwords, idx + rowL, lane);
+          if (lane == 0) R_out[b] = R;
+        }
       }
     }
   } else {
@@ -214,7 +311,7 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
         nvalid_local += ok ? 1 : 0;
       }
     }
-    nD = min(n_dec, block_sum_int(nvalid_local, sh));  // contains __syncthreads
+    const int nD = min(n_dec, block_sum_int(nvalid_local, sh));  // contains __syncthreads
 #pragma unroll
     for (int q = 0; q < kPerThread; ++q) {
       const int i = tid + q * kThreads;
@@ -230,6 +327,8 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
       }
     }
     __syncthreads();
+    float emax = -INFINITY;
+    int any_nan = 0;
 #pragma unroll
     for (int q = 0; q < kPerThread; ++q) {
       const int i = tid + q * kThreads;
@@ -252,51 +351,47 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
         else emax = fmaxf(emax, h);
       }
     }
-  }
+    for (int t = nD + tid; t < n_dec; t += kThreads) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
-    any_nan |= __shfl_xor_sync(0xffffffffu, any_nan, off);
-  }
-  if (lane == 0) {
-    sh.warp_e[warp] = emax;
-    sh.warp_nan[warp] = any_nan;
-  }
-  if (tid == 0) sh.nd = nD;  // thread 0 is in warp 0, which knows nD on both paths
-  __syncthreads();
-  if (tid == 0) {
-    const int nd = sh.nd;
-    float e = -INFINITY;
-    int nan_seen = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      e = fmaxf(e, sh.warp_e[w]);
-      nan_seen |= sh.warp_nan[w];
+    for (int off = 16; off > 0; off >>= 1) {
+      emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, off));
+      any_nan |= __shfl_xor_sync(0xffffffffu, any_nan, off);
     }
-    float E;
-    int full;
-    if (nd == 0) {
-      E = 0.f;  // nothing decoded: E = 0
-      full = (E > tau) ? 1 : 0;
-    } else if (nan_seen) {
-      E = NAN;
-      full = 1;
-    } else {
-      E = e;
-      full = (E > tau) ? 1 : 0;
+    if (lane == 0) {
+      sh.warp_e[warp] = emax;
+      sh.warp_nan[warp] = any_nan;
     }
-    E_out[b] = E;
-    flag_out[b] = static_cast<uint8_t>(full);
-    const int head1 = (head0 + nd) % k;
-    const int count1 = min(sh.count + nd, k);
-    ring_head[b] = head1;
-    ring_count[b] = count1;
-    sh.head = head1;
-    sh.count = count1;
-    sh.full = full;
-    sh.carry = 0;
+    __syncthreads();
+    if (tid == 0) {
+      float e = -INFINITY;
+      int nan_seen = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        e = fmaxf(e, sh.warp_e[w]);
+        nan_seen |= sh.warp_nan[w];
+      }
+      const float E = nD == 0 ? 0.f : (nan_seen ? NAN : e);  // nothing decoded: E = 0
+      const int full = (nD > 0 && nan_seen) ? 1 : (E > tau ? 1 : 0);
+      E_out[b] = E;
+      flag_out[b] = static_cast<uint8_t>(full);
+      const int head1 = (head0 + nD) % k;
+      const int count1 = min(sh.count + nD, k);
+      ring_head[b] = head1;
+      ring_count[b] = count1;
+      sh.head = head1;
+      sh.count = count1;
+      sh.full = full;
+    }
+    __syncthreads();
+    if (!sh.full) {
+      const int head1 = sh.head, count1 = sh.count;
+      for (int t = tid; t < count1; t += kThreads) {  // the last min(k, count) decoded positions
+        const int q = rs[((head1 - 1 - t) % k + k) % k];
+        if (q >= 0 && q < L) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
+        else report_error(dev_err, EC_DEVERR_BAD_IDX);
+      }
+    }
   }
   __syncthreads();
-  for (int t = sh.nd + tid; t < n_dec; t += kThreads) dec_pos[static_cast<int64_t>(b) * n_dec + t] = -1;
 
   // ---- phase D: the recompute set ------------------------------------------------------------
   if (sh.full) {
@@ -304,14 +399,7 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(
     if (tid == 0) R_out[b] = L;
     return;
   }
-  const int nwords = (L + 31) >> 5;
-  const int head1 = sh.head, count1 = sh.count;
-  for (int t = tid; t < count1; t += kThreads) {  // the last min(k, count) decoded positions
-    const int p = rs[((head1 - 1 - t) % k + k) % k];
-    if (p >= 0 && p < L) atomicOr(&bitmap[p >> 5], 1u << (p & 31));
-    else report_error(dev_err, EC_DEVERR_BAD_IDX);
-  }
-  __syncthreads();
+  if (fast && nwords <= 32) return;  // warp 0 has compacted already
   for (int base = 0; base < nwords; base += kThreads) {
     const int w = base + tid;
     const uint32_t bits = (w < nwords) ? bitmap[w] : 0u;

@@ -121,6 +121,7 @@ def test_llada_trace_256_steps_32_layers():
     frac = n_full / (w.steps * w.B)
     print(f"trace: {n_full} full of {w.steps * w.B} (step, sequence) pairs ({frac:.3f}), {n_exempt} exemptions")
     assert 0.03 <= frac <= 0.25
+    assert n_exempt == 0  # the workload keeps every decision clear of the exemption margins
     # the caches of the sampled layers match the oracle's after the whole trace
     for l in SAMPLED_LAYERS:
         np.testing.assert_array_equal(bf16_bits(layers[l]["k_cache"]), host[l]["k_cache"])

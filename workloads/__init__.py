@@ -24,10 +24,10 @@ Logit distributions:
                logit = -1.1 ln rho + N(0, 1)
   trace        per (step, sequence) a Bernoulli(0.1) draw (step 0 always high) picks
                high: every row N(0, 0.5^2)  (entropy about ln V)
-               low:  every row N(0, 1) plus a peak at one seeded token; with c candidate
-                     rows this step (c = 32 - step mod 32), row i's peak is
-                     17.25 - 0.25 (c - 1 - i), so the most confident row has entropy about 0.05
-                     and the confidences of the best rows lie ~1e-3 apart
+               low:  every row N(0, 1) except one seeded token set to a peak; with c
+                     candidate rows this step (c = 32 - step mod 32), row i's peak is exactly
+                     17.25 - 0.25 (c - 1 - i) (exact in bf16), so the most confident row has
+                     entropy about 0.05 and the best rows' confidences differ by ~25%
 K/V cache, queries ~ N(0, 1); fresh K/V rows = cache + N(0, 0.05^2); all bf16.
 """
 from __future__ import annotations
@@ -223,7 +223,7 @@ def step_logits(w: Workload, step: int = 0) -> np.ndarray:
                 peak = r.integers(0, V, size=C)
                 c = w.block - step % w.block
                 height = 17.25 - 0.25 * (c - 1 - np.arange(C))
-                out[b, np.arange(C), peak] += height.astype(np.float32)
+                out[b, np.arange(C), peak] = height.astype(np.float32)
         else:
             raise ValueError(w.logits_kind)
     return _finish_logits(w, out)

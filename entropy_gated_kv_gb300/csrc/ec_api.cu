@@ -221,11 +221,10 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
   auto* conf = reinterpret_cast<float*>(w + lay.conf);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  const int32_t rows = p->B * p->C_max;
-  cudaError_t e = launch_entropy_decode(logits, p->V, rows, p->V, p->logits_dtype, ids, ent, conf, w + lay.k1,
-                                        cand_count, p->C_max, s);
-  if (e != cudaSuccess) return EC_ERR_CUDA;
-  e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, s);
+  // stages (a)-(c): decode + entropy of the candidate rows, then the select stage
+  cudaError_t e = launch_entropy_decode(logits, p->V, p->B * p->C_max, p->V, p->logits_dtype, ids, ent, conf,
+                                        w + lay.k1, cand_count, p->C_max, s);
+  if (e == cudaSuccess) e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, s);
   if (e != cudaSuccess) return EC_ERR_CUDA;
   for (int32_t l = 0; l < n_layers; ++l) {
     e = launch_kv_scatter(*p, k_cache[l], v_cache[l], k_src[l], v_src[l], 1, st->idx, st->R, q_src[l],

@@ -30,6 +30,10 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
                                   const int32_t* row_count, int32_t rows_per_group, cudaStream_t s);
 
 // ---- select_recompute ---------------------------------------------------------------------
+struct SelArgs;
+SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
+                      const int32_t* ids, const float* entropy, const float* log_conf);
+size_t select_smem_bytes(const ec_params& p);
 cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
                                     const int32_t* cand_count, const int32_t* ids, const float* entropy,
                                     const float* log_conf, cudaStream_t s);

@@ -177,25 +177,35 @@ __device__ __forceinline__ void write_row(int row, float m_unused, int idx, floa
   log_conf[row] = -kLn2 * l2s;
 }
 
+struct EntArgs {
+  const char* logits;
+  int64_t row_stride_bytes;
+  int32_t V, nchunks;
+  int32_t* ids;
+  float* entropy;
+  float* log_conf;
+  ChunkPartial* partials;
+  uint32_t* counters;
+  const int32_t* row_count;
+  int32_t rows_per_group;
+};
+
+// One (row, vocabulary chunk) per CTA. Returns the row whose final result this CTA wrote (the
+// only chunk of the row, or its last chunk to finish), else -1. Uniform over the CTA.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) entropy_decode_kernel(
-    const char* __restrict__ logits, int64_t row_stride_bytes, int32_t V, int32_t nchunks,
+__device__ __forceinline__ int entropy_chunk(
+    int64_t bid, const char* __restrict__ logits, int64_t row_stride_bytes, int32_t V, int32_t nchunks,
     int32_t* __restrict__ ids, float* __restrict__ entropy, float* __restrict__ log_conf,
     ChunkPartial* __restrict__ partials, uint32_t* __restrict__ counters, const int32_t* __restrict__ row_count,
-    int32_t rows_per_group) {
+    int32_t rows_per_group, BlockScratch& sh) {
   constexpr int PV = Elem<DT>::kPerVec;
   constexpr int EB = Elem<DT>::kBytes;
   constexpr int CE = chunk_elems<DT>();
-  __shared__ BlockScratch sh;
-
-  const int64_t bid = blockIdx.x;
   const int row = static_cast<int>(bid / nchunks);
   const int chunk = static_cast<int>(bid - static_cast<int64_t>(row) * nchunks);
-  pdl_wait();  // logits and row counts may come from the previous kernel in the stream
-  pdl_launch_dependents();
   if (row_count != nullptr) {
     const int grp = row / rows_per_group;
-    if (row - grp * rows_per_group >= __ldg(row_count + grp)) return;  // whole row skipped
+    if (row - grp * rows_per_group >= __ldg(row_count + grp)) return -1;  // whole row skipped
   }
   const char* rowp = logits + static_cast<int64_t>(row) * row_stride_bytes;
   const int64_t c0 = static_cast<int64_t>(chunk) * CE;
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kThreads) entropy_decode_kernel(
 
   if (nchunks == 1) {
     if (threadIdx.x == 0) write_row(row, m, mi, S, T, ids, entropy, log_conf);
-    return;
+    return row;
   }
 
   // Publish this chunk; the last chunk of the row to finish merges.
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kThreads) entropy_decode_kernel(
     sh.last = (done == static_cast<uint32_t>(nchunks - 1)) ? 1 : 0;
   }
   __syncthreads();
-  if (!sh.last) return;
+  if (!sh.last) return -1;
   __threadfence();
 
   const ChunkPartial* rp = partials + static_cast<int64_t>(row) * nchunks;
@@ -308,6 +318,16 @@ __global__ void __launch_bounds__(kThreads) entropy_decode_kernel(
     write_row(row, rm, ri, RS, RT, ids, entropy, log_conf);
     counters[row] = 0u;  // ready for the next call
   }
+  return row;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) entropy_decode_kernel(EntArgs a) {
+  __shared__ BlockScratch sh;
+  pdl_wait();  // logits and row counts may come from the previous kernel in the stream
+  pdl_launch_dependents();
+  entropy_chunk<DT>(blockIdx.x, a.logits, a.row_stride_bytes, a.V, a.nchunks, a.ids, a.entropy, a.log_conf,
+                    a.partials, a.counters, a.row_count, a.rows_per_group, sh);
 }
 
 }  // namespace
@@ -339,12 +359,10 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   const int64_t nblocks = static_cast<int64_t>(n_rows) * nch;
   if (nblocks > INT_MAX) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(nblocks));
-  const char* lg = static_cast<const char*>(logits);
-  if (dtype == EC_F32)
-    return launch_pdl(entropy_decode_kernel<EC_F32>, grid, dim3(kThreads), 0, s, lg, row_stride * 4, V, nch, ids,
-                      entropy, log_conf, partials, counters, row_count, rows_per_group);
-  return launch_pdl(entropy_decode_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, lg, row_stride * 2, V, nch, ids,
-                    entropy, log_conf, partials, counters, row_count, rows_per_group);
+  const EntArgs a{static_cast<const char*>(logits), row_stride * (dtype == EC_F32 ? 4 : 2), V, nch, ids, entropy,
+                  log_conf, partials, counters, row_count, rows_per_group};
+  if (dtype == EC_F32) return launch_pdl(entropy_decode_kernel<EC_F32>, grid, dim3(kThreads), 0, s, a);
+  return launch_pdl(entropy_decode_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, a);
 }
 
 }  // namespace ec

@@ -167,6 +167,14 @@ class ClockSampler:
 # our arm
 
 
+def bench_workload(args):
+    """The workload timed: workload 2 by default; --workload / --tau override it."""
+    w = W.workload(args.workload)
+    if args.tau is not None:
+        w = w.scaled(tau=float(args.tau))
+    return w
+
+
 def run_ours(args, rank: int, world: int) -> dict | None:
     import torch
 
@@ -176,7 +184,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     B.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w = W.workload(WORKLOAD)
+    w = bench_workload(args)
     p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
                  logits_dtype=w.logits_dtype)
     K, Wm = args.steps, args.warmup
@@ -188,7 +196,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     base = {n: bf(lay_h[n]) for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
-    base["logits"] = bf(lg_h)
+    base["logits"] = bf(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(lg_h).to(dev)
     copies = []
     for c in range(NCOPY):
         d = {n: t.clone() for n, t in base.items()}
@@ -231,8 +239,8 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     status, word = E.read_device_error(st0.dev_err)
     if status != 0:
         raise RuntimeError(f"device error word {word:#x} during warm-up")
-    flag = int(st0.flag[0].item())
-    R = int(st0.R[0].item())
+    flag = int(st0.flag.max().item())
+    R = int(st0.R.sum().item())
 
     def capture(n):
         g = torch.cuda.CUDAGraph()
@@ -276,10 +284,13 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     if status != 0:
         raise RuntimeError(f"device error word {word:#x} during the timed steps")
 
-    res = {"ms": ms, "flag": flag, "R": R, "clocks": clk.summary()}
+    copy_mb = sum(t.numel() * t.element_size() for t in copies[0].values()) / 1e6
+    res = {"ms": ms, "flag": flag, "R": R, "clocks": clk.summary(), "copy_mb": copy_mb}
     if rank == 0:
         res["kernels"] = time_kernels(E, p, w, copies, st0, dev, min(K, 2000))
-        res["e2e"] = run_e2e(E, p, w, lay_h, lg_h, st_h, dev, min(K, 2000))
+        per_step = sum(lay_h[n].nbytes for n in ("k_src", "v_src", "q_src")) + lg_h.nbytes
+        n_e2e = max(10, min(K, 2000, int(20e9 // per_step)))  # at most ~20 GB of host->device traffic
+        res["e2e"] = run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n_e2e)
     del g_main, g_rem
     return res
 
@@ -345,7 +356,7 @@ def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
     out["entropy_decode_us"] = timed(stage_entropy, n)
     out["partial_attention_us"] = timed(stage_attention, n)
     out["kv_scatter_us"] = timed(stage_scatter, n)
-    out["R"] = int(R[0].item())
+    out["R"] = int(R.sum().item())  # recompute rows over the batch
     return out
 
 
@@ -359,8 +370,8 @@ def run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n) -> dict:
         return t.pin_memory()
 
     h = {n: pinned(lay_h[n]) for n in ("k_src", "v_src", "q_src")}
-    h["logits"] = pinned(lg_h)
-    d = {n: torch.empty(t.shape, dtype=torch.int16, device=dev) for n, t in h.items()}
+    h["logits"] = pinned(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(lg_h).pin_memory()
+    d = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in h.items()}
     kc = torch.from_numpy(lay_h["k_cache"].view(np.int16)).to(dev)
     vc = torch.from_numpy(lay_h["v_cache"].view(np.int16)).to(dev)
     out = torch.empty(w.B, w.L, w.Hq, w.D, dtype=torch.int16, device=dev)
@@ -381,7 +392,7 @@ def run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n) -> dict:
             getattr(st, f).copy_(getattr(pristine, f), non_blocking=True)
         for k_, t in h.items():
             d[k_].copy_(t, non_blocking=True)
-        E.step(p, st, d["logits"].view(bf), cand_pos, cand_count,
+        E.step(p, st, d["logits"].view(bf) if w.logits_dtype == "bf16" else d["logits"], cand_pos, cand_count,
                [dict(k_cache=kc.view(bf), v_cache=vc.view(bf), k_src=d["k_src"].view(bf), v_src=d["v_src"].view(bf),
                      q_src=d["q_src"].view(bf), out=out.view(bf))], ws=ws)
         out_h.copy_(out, non_blocking=True)
@@ -404,20 +415,20 @@ def run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n) -> dict:
 
 
 def algorithmic(w, R) -> dict:
-    """Algorithmic bytes / flops per launch of each stage."""
+    """Algorithmic bytes / flops per launch of each stage; R = recompute rows over the batch."""
     esz = 2 if w.logits_dtype == "bf16" else 4
     kv_row = w.Hkv * w.D * 2
     q_row = w.Hq * w.D * 2
     return {
         "entropy_decode_bytes": w.B * w.C_max * w.V * esz + w.B * w.C_max * 12,
-        "partial_attention_bytes": w.B * (2 * w.L * kv_row + 2 * R * q_row),
-        "partial_attention_flops": 4 * w.B * w.Hq * R * w.L * w.D,
-        "kv_scatter_bytes": w.B * R * (4 * kv_row + 2 * q_row),
+        "partial_attention_bytes": w.B * 2 * w.L * kv_row + 2 * R * q_row,
+        "partial_attention_flops": 4 * w.Hq * R * w.L * w.D,
+        "kv_scatter_bytes": R * (4 * kv_row + 2 * q_row),
     }
 
 
 def emit_ours(args, res, rank, world):
-    w = W.workload(WORKLOAD)
+    w = bench_workload(args)
     pk = peaks()
     K = args.steps
     ms_per_step = res["ms"] / K
@@ -428,18 +439,21 @@ def emit_ours(args, res, rank, world):
     att_gbs = alg["partial_attention_bytes"] / (kern["partial_attention_us"] * 1e-6) / 1e9
     att_tfs = alg["partial_attention_flops"] / (kern["partial_attention_us"] * 1e-6) / 1e12
     sc_gbs = alg["kv_scatter_bytes"] / (kern["kv_scatter_us"] * 1e-6) / 1e9
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    att_tensor = alg["partial_attention_flops"] / alg["partial_attention_bytes"] > ridge
+    att_roof = ({"bound": "tensor", "achieved": att_tfs, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"} if att_tensor
+                else {"bound": "hbm", "achieved": att_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s"})
     cands = {
         "entropy_decode": (kern["entropy_decode_us"], {"bound": "hbm", "achieved": ent_gbs, "peak": pk["hbm_gbs"],
                                                        "unit": "GB/s"}),
-        "partial_attention": (kern["partial_attention_us"], {"bound": "hbm", "achieved": att_gbs,
-                                                             "peak": pk["hbm_gbs"], "unit": "GB/s"}),
+        "partial_attention": (kern["partial_attention_us"], att_roof),
     }
     dom = max(cands, key=lambda k_: cands[k_][0])
     roof = dict(cands[dom][1])
     roof["kernel"] = dom
     roof["frac"] = roof["achieved"] / roof["peak"]
     src = {"entropy_decode": "entropy_decode.cu", "partial_attention": "attention.cu"}[dom]
-    roof["traffic"] = profiled_traffic(dom, src)
+    roof["traffic"] = profiled_traffic(dom, src) if args.workload == WORKLOAD and args.tau is None else None
     roof["peak_source"] = pk["source"] + " (burst; kernel timed alone)"
     line = {
         "metric": METRIC,
@@ -454,8 +468,8 @@ def emit_ours(args, res, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": workload_desc(w), "step": f"{'full' if res['flag'] else 'partial'} (R={res['R']})",
-                   "l2": f"inputs rotate over {NCOPY} copies ({NCOPY} x 58 MB > 129 MB L2)",
+        "config": {"workload": workload_desc(w), "step": f"{'full' if res['flag'] else 'partial'} (R={res['R']} over the batch)",
+                   "l2": f"inputs rotate over {NCOPY} copies ({NCOPY} x {res['copy_mb']:.0f} MB; L2 is 129 MB)",
                    "timing": f"CUDA graphs of {min(CHUNK, K)} steps, state restore inside"},
         "roofline": roof,
         "kernels": {
@@ -587,6 +601,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 5],
+                    help="workload to time (default 2, the LLaDA-8B layer step)")
+    ap.add_argument("--tau", type=float, default=None, help="override tau (e.g. -1 forces a full step)")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many eager steps and exit (a short program for ncu)")
     args = ap.parse_args()

@@ -9,14 +9,14 @@
 //
 // Structure (one CTA per SM, persistent, 6 warps):
 //   warp 0      TMA producer: the query tile once per work item, then K and V blocks of
-//               128 keys into a 2-stage ring (128-byte swizzle, mbarrier transaction counts).
+//               128 keys into a 3-stage ring (128-byte swizzle, mbarrier transaction counts).
 //   warp 1      allocates 512 TMEM columns; one lane issues tcgen05.mma: S = Q K^T into one
-//               of two TMEM S buffers, and O += P V into the TMEM O accumulator; completion
-//               is signalled with tcgen05.commit on mbarriers.
+//               of three TMEM S buffers, and O += P V into the TMEM O accumulator with P read
+//               from TMEM; completion is signalled with tcgen05.commit on mbarriers.
 //   warps 2..5  softmax and epilogue, one TMEM lane (= one packed query row) per thread:
 //               tcgen05.ld of the S row, online softmax in base 2 with a lazy rescale of O
-//               (only when the running max grows by more than 2^8), P in bf16 written to
-//               shared memory in the swizzled K-major layout the next MMA reads.
+//               (only when the running max grows by more than 2^8), P in bf16 written back
+//               over the first half of the S buffer with tcgen05.st (no shared memory).
 // Grouped-query attention packs the g = Hq / Hkv query heads of one KV head into the 128 MMA
 // rows (floor(128 / g) query rows per tile), so K/V are read once per KV head.
 // Work items (b, kv head, row tile, KV split) are derived on the device from R[], so the
@@ -44,8 +44,9 @@ constexpr int kBlockM = 128;  // packed query rows per tile (TMEM lanes)
 constexpr int kBlockN = 128;  // keys per KV block
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;    // S buffers at columns [0, 128) and [128, 256)
-constexpr uint32_t kTmemO = 256;  // O accumulator at columns [256, 256 + D)
+constexpr int kStages = 3;        // K/V blocks in flight, and S/P buffers in TMEM
+constexpr uint32_t kTmemS = 0;    // S buffer i at columns [128 i, 128 i + 128); P (bf16) over its first 64
+constexpr uint32_t kTmemO = 384;  // O accumulator at columns [384, 384 + D)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxGrid = 256;
@@ -54,10 +55,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
 struct Bars {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], p_free[2];
-  uint64_t pv_done, o_full, o_free;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[kStages], s_free[kStages];  // s_free: the PV product that read P from the buffer is done
+  uint64_t p_full[kStages];
+  uint64_t o_full, o_free;
   uint64_t recv;  // split merge: bytes pushed into this CTA by its cluster peers
   uint32_t tmem_base;
   int abort;
@@ -70,11 +71,9 @@ struct Layout {
   static constexpr int kQBytes = kAtoms * kAtomBytes;
   static constexpr int kKVBytes = kAtoms * kAtomBytes;   // one of K or V for one block
   static constexpr int kStageBytes = 2 * kKVBytes;
-  static constexpr int kPBytes = 2 * kAtomBytes;         // 128 rows x 128 keys
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = kQOff + kQBytes;
-  static constexpr int kPOff = kStageOff + 2 * kStageBytes;
-  static constexpr int kBarOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
   static constexpr int kBytes = kBarOff + static_cast<int>(sizeof(Bars));
   static constexpr int kDynSmem = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -193,15 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 128);
+      mbar_init(&bars->s_free[i], 1);
       mbar_init(&bars->p_full[i], 128);
-      mbar_init(&bars->p_free[i], 1);
     }
-    mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, 128);
     mbar_init(&bars->recv, 1);
@@ -247,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
             tma_load_5d(q_smem + a * LY::kAtomBytes, &tm_q, &bars->q_full, a * 64, 0, I.kvh, I.r0, I.b);
         }
         for (int j = 0; ok && j < I.nblk; ++j) {
-          const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+          const uint32_t cur = it + j, slot = cur % kStages, u = cur / kStages;
           ok = mbar_wait_bounded(&bars->kv_empty[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
           if (!ok) break;
           uint8_t* kst = smem + LY::kStageOff + slot * LY::kStageBytes;
@@ -278,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
         ok = mbar_wait_bounded(&bars->q_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
         for (int j = 0; ok && j <= I.nblk; ++j) {
           if (j < I.nblk) {
-            const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+            const uint32_t cur = it + j, slot = cur % kStages, u = cur / kStages;
             ok = mbar_wait_bounded(&bars->kv_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs) &&
                  mbar_wait_bounded(&bars->s_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
             if (!ok) break;
@@ -294,24 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
             if (j == I.nblk - 1) umma_commit(&bars->q_empty);
           }
           if (j >= 1) {
-            const uint32_t prev = it + j - 1, ps = prev & 1u, pu = prev >> 1;
+            const uint32_t prev = it + j - 1, ps = prev % kStages, pu = prev / kStages;
             if (j == 1 && n > 0)
               ok = mbar_wait_bounded(&bars->o_free, (n - 1) & 1, abort_flag, dev_err, kWaitLimitNs);
             ok = ok && mbar_wait_bounded(&bars->p_full[ps], pu & 1u, abort_flag, dev_err, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t p_addr = smem_u32(smem + LY::kPOff + ps * LY::kPBytes);
             const uint32_t v_addr = smem_u32(smem + LY::kStageOff + ps * LY::kStageBytes + LY::kKVBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
-              const uint32_t a_off = (kk >> 2) * LY::kAtomBytes + (kk & 3) * 32;
-              umma_bf16(tmem + kTmemO, smem_desc_sw128(p_addr + a_off, 16, 1024),
-                        smem_desc_sw128(v_addr + kk * 2048, LY::kAtomBytes, 1024), idesc_pv,
-                        (j > 1 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kBlockN / 16; ++kk)  // P: 16 keys = 8 TMEM columns per product
+              umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + ps * kBlockN + kk * 8,
+                           smem_desc_sw128(v_addr + kk * 2048, LY::kAtomBytes, 1024), idesc_pv,
+                           (j > 1 || kk > 0) ? 1u : 0u);
             umma_commit(&bars->kv_empty[ps]);
-            umma_commit(&bars->p_free[ps]);
-            umma_commit(&bars->pv_done);
+            umma_commit(&bars->s_free[ps]);
             if (j == I.nblk) umma_commit(&bars->o_full);
           }
         }
@@ -323,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     // ------------------------------------------------------------------ softmax + epilogue
     const int row = 32 * (warp & 3) + lane;  // TMEM lane = packed query row
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    uint8_t* const p_row0 = smem + LY::kPOff + row * 128;
     uint32_t it = 0;
     bool staged = false;
     for (int n = 0;; ++n) {
@@ -334,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true;
       for (int j = 0; j < I.nblk; ++j) {
-        const uint32_t cur = it + j, slot = cur & 1u, u = cur >> 1;
+        const uint32_t cur = it + j, slot = cur % kStages, u = cur / kStages;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[slot], u & 1u, abort_flag, dev_err, kWaitLimitNs));
         if (!ok) break;
         tc_fence_after();
@@ -342,8 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
 #pragma unroll
         for (int c = 0; c < kBlockN / 32; ++c) EC_TMEM_LD32(tmem + lane_off + kTmemS + slot * kBlockN + c * 32, (sr + c * 32));
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bars->s_free[slot]);
 
         // Row max of the raw scores (scale > 0 commutes with max), 8 independent chains.
         const int nvalid = min(kBlockN, I.kv_end - (I.kb0 + j) * kBlockN);
@@ -386,27 +376,18 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
         }
         const float rs = ((rss[0] + rss[1]) + (rss[2] + rss[3])) + ((rss[4] + rss[5]) + (rss[6] + rss[7]));
         l_sum += rs;
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait_bounded(&bars->p_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs));
-        if (!ok) break;
-        uint8_t* prow = p_row0 + slot * LY::kPBytes;
-#pragma unroll
-        for (int c = 0; c < kBlockN / 8; ++c) {  // 16-byte chunk c holds keys 8c .. 8c+7
-          const int atom = c >> 3, ch = c & 7;
-          uint4 v;
-          v.x = pk[4 * c + 0];
-          v.y = pk[4 * c + 1];
-          v.z = pk[4 * c + 2];
-          v.w = pk[4 * c + 3];
-          *reinterpret_cast<uint4*>(prow + atom * LY::kAtomBytes + ((ch ^ (row & 7)) << 4)) = v;
-        }
-        fence_proxy_async_smem();
+        // P (bf16) over the first 64 columns of this S buffer: the PV product reads it from TMEM.
+        EC_TMEM_ST32(tmem + lane_off + kTmemS + slot * kBlockN, pk);
+        EC_TMEM_ST32(tmem + lane_off + kTmemS + slot * kBlockN + 32, (pk + 32));
+        tmem_wait_st();
         // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
         // needs it (alpha = 1 for the others).
         if (__any_sync(0xffffffffu, rescale)) {
-          // O holds the products of blocks 0 .. j-1; wait for the last of them, then scale.
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait_bounded(&bars->pv_done, (cur - 1) & 1u, abort_flag, dev_err, kWaitLimitNs));
+          // O holds the products of blocks 0 .. j-1; wait for the last of them (its buffer's
+          // release), then scale.
+          const uint32_t prev = cur - 1;
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_free[prev % kStages], (prev / kStages) & 1u, abort_flag,
+                                                         dev_err, kWaitLimitNs));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll

@@ -239,6 +239,11 @@ EC_DEV uint32_t cluster_count_x() {
   return r;
 }
 // Every thread of every CTA of the cluster (warp-aligned).
+EC_DEV uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
 EC_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

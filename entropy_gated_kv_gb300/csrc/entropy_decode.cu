@@ -7,17 +7,25 @@
 //   entropy[i] = -sum_j p_ij ln p_ij,  p_ij = softmax_j(x_ij)
 //   log_conf[i] = ln p_{i, ids[i]} = -ln S_i,  S_i = sum_j exp(x_ij - max)
 //
-// Design (HBM-bound: every logit is read exactly once).
-//   - Split-V: the row is cut into chunks of kThreads * kVecPerThread 16-byte vectors; one
-//     CTA per (row, chunk), so a 32 x 126464 bf16 problem runs as 512 CTAs and issues all of
-//     its loads in the first wave. Each thread issues all its 16-byte streaming loads before
-//     any arithmetic.
-//   - Two passes over registers: (1) max and lowest index over the raw stored values (exact,
-//     no rescaling before comparison), block-reduced; (2) S = sum 2^d and T = sum d 2^d with
-//     d = (x - M) log2(e) relative to the block max M, block-reduced. H = ln2 (log2 S - T/S).
-//   - Chunks of a row merge in the last CTA to finish (a counter per row, no spinning): it
-//     rescales every chunk's (S, T) to the row max, picks the row argmax with the
-//     lower-index tie rule, writes the row result and returns the counter to zero.
+// Design (HBM-bound: every logit is read exactly once; at the sizes of one decoding step the
+// kernel's latency matters as much as its bandwidth). Two launch shapes share the per-stretch
+// reduction (sub_chunk):
+//   - Two passes over registers per stretch: (1) max and lowest index over the raw stored
+//     values (exact, no rescaling before comparison), block-reduced; (2) S = sum 2^d and
+//     T = sum d 2^d with d = (x - M) log2(e) relative to the stretch max M, block-reduced.
+//     Stretches combine by rescaling S and T to the larger max (part_merge).
+//     H = ln2 (log2 S - T/S). Each thread issues all its 16-byte streaming loads of a
+//     stretch before any arithmetic.
+//   - Few rows (the whole problem within about one wave): one thread-block cluster of up to
+//     8 CTAs per row, CTA r owning a contiguous slice of the row; the slices merge on chip:
+//     each CTA leaves its (max, index, S, T) in shared memory and, after one cluster barrier,
+//     the first CTA reads them through distributed shared memory and writes the row result.
+//     A 32 x 126464 bf16 problem runs as 256 CTAs with one global round trip.
+//   - Many rows: one CTA per (row, 8192-element chunk), so every load is in flight at once;
+//     each chunk publishes its partial to the workspace and the last chunk of a row to finish
+//     (a counter per row, no spinning) merges them, writes the row result and returns the
+//     counter to zero.
+#include <algorithm>
 #include <climits>
 
 #include "ec_common.cuh"
@@ -27,7 +35,10 @@ namespace ec {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kVecPerThread = 4;
+constexpr int kSplitVec = 4;    // 16-byte vectors per thread, one CTA per (row, chunk)
+constexpr int kClusterVec = 8;  // 16-byte vectors per thread per stretch, cluster path
+constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
+constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs
 constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -46,8 +57,8 @@ struct Elem<EC_BF16> {
 };
 
 template <int DT>
-constexpr int chunk_elems() {
-  return kThreads * kVecPerThread * Elem<DT>::kPerVec;
+constexpr int chunk_elems() {  // the split path's chunk (the workspace is sized by it)
+  return kThreads * kSplitVec * Elem<DT>::kPerVec;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -180,44 +191,67 @@ __device__ __forceinline__ void write_row(int row, float m_unused, int idx, floa
 struct EntArgs {
   const char* logits;
   int64_t row_stride_bytes;
-  int32_t V, nchunks;
+  int32_t V, nchunks;  // nchunks: split path only
   int32_t* ids;
   float* entropy;
   float* log_conf;
-  ChunkPartial* partials;
-  uint32_t* counters;
+  ChunkPartial* partials;  // split path only
+  uint32_t* counters;      // split path only
   const int32_t* row_count;
   int32_t rows_per_group;
 };
 
-// One (row, vocabulary chunk) per CTA. Returns the row whose final result this CTA wrote (the
-// only chunk of the row, or its last chunk to finish), else -1. Uniform over the CTA.
-template <int DT>
-__device__ __forceinline__ int entropy_chunk(
-    int64_t bid, const char* __restrict__ logits, int64_t row_stride_bytes, int32_t V, int32_t nchunks,
-    int32_t* __restrict__ ids, float* __restrict__ entropy, float* __restrict__ log_conf,
-    ChunkPartial* __restrict__ partials, uint32_t* __restrict__ counters, const int32_t* __restrict__ row_count,
-    int32_t rows_per_group, BlockScratch& sh) {
+// Rows past their group's count are skipped (uniform over a CTA and over a cluster).
+__device__ __forceinline__ bool row_skipped(const EntArgs& a, int row) {
+  if (a.row_count == nullptr) return false;
+  const int grp = row / a.rows_per_group;
+  return row - grp * a.rows_per_group >= __ldg(a.row_count + grp);
+}
+
+// (max, index, S, T) of a stretch of one row, S and T relative to its own max (log2 units).
+struct Part {
+  float m;
+  int i;
+  float s;
+  float t;
+};
+
+// Adds stretch b to stretch a: argmax with the lower-index rule (also over stretches whose
+// values are all -inf), S and T rescaled to the larger max. S >= 1 whenever a stretch's max
+// is finite (its maximum contributes 2^0), so S == 0 marks a stretch without mass.
+__device__ __forceinline__ void part_merge(Part& a, const Part& b) {
+  float m = a.m;
+  int i = a.i;
+  argmax_merge(m, i, b.m, b.i);
+  if (b.s > 0.f) {
+    if (a.s > 0.f) {
+      const float da = (a.m - m) * kLog2e, db = (b.m - m) * kLog2e;
+      const float fa = ex2_approx(da), fb = ex2_approx(db);
+      a.t = fa * fmaf(da, a.s, a.t) + fb * fmaf(db, b.s, b.t);
+      a.s = fa * a.s + fb * b.s;
+    } else {
+      a.s = b.s;
+      a.t = b.t;
+    }
+  }
+  a.m = m;
+  a.i = i;
+}
+
+// One stretch [c0, c1) of a row (c0 a multiple of the vector width, at most NV vectors per
+// thread plus a tail of fewer than one vector at the row's end); uniform over the CTA.
+template <int DT, int NV>
+__device__ __forceinline__ Part sub_chunk(const char* __restrict__ rowp, int64_t c0, int64_t c1, BlockScratch& sh) {
   constexpr int PV = Elem<DT>::kPerVec;
   constexpr int EB = Elem<DT>::kBytes;
-  constexpr int CE = chunk_elems<DT>();
-  const int row = static_cast<int>(bid / nchunks);
-  const int chunk = static_cast<int>(bid - static_cast<int64_t>(row) * nchunks);
-  if (row_count != nullptr) {
-    const int grp = row / rows_per_group;
-    if (row - grp * rows_per_group >= __ldg(row_count + grp)) return -1;  // whole row skipped
-  }
-  const char* rowp = logits + static_cast<int64_t>(row) * row_stride_bytes;
-  const int64_t c0 = static_cast<int64_t>(chunk) * CE;
-  const int64_t c1 = min(static_cast<int64_t>(V), c0 + CE);
   const int nvec = static_cast<int>((c1 - c0) / PV);
   const int64_t tail0 = c0 + static_cast<int64_t>(nvec) * PV;
   const int ntail = static_cast<int>(c1 - tail0);
 
   // Issue every load of this thread before any arithmetic.
-  uint4 v[kVecPerThread];
+  uint4 v[NV];
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
+  for (int u = 0; u < NV; ++u) {
     const int vi = threadIdx.x + u * kThreads;
     if (vi < nvec) v[u] = ld_stream_v4(rowp + (c0 + static_cast<int64_t>(vi) * PV) * EB);
   }
@@ -229,7 +263,7 @@ __device__ __forceinline__ int entropy_chunk(
   float m = -INFINITY;
   int mi = INT_MAX;
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
+  for (int u = 0; u < NV; ++u) {
     const int vi = threadIdx.x + u * kThreads;
     if (vi < nvec) {
       float x[PV];
@@ -255,7 +289,7 @@ __device__ __forceinline__ int entropy_chunk(
   const float M2 = m * kLog2e;
   float S = 0.f, T = 0.f;
 #pragma unroll
-  for (int u = 0; u < kVecPerThread; ++u) {
+  for (int u = 0; u < NV; ++u) {
     const int vi = threadIdx.x + u * kThreads;
     if (vi < nvec) {
       float x[PV];
@@ -276,58 +310,100 @@ __device__ __forceinline__ int entropy_chunk(
     T = fmaf(p, d, T);
   }
   block_sum2(S, T, sh);
-
-  if (nchunks == 1) {
-    if (threadIdx.x == 0) write_row(row, m, mi, S, T, ids, entropy, log_conf);
-    return row;
-  }
-
-  // Publish this chunk; the last chunk of the row to finish merges.
-  if (threadIdx.x == 0) {
-    partials[static_cast<int64_t>(row) * nchunks + chunk] = ChunkPartial{m, mi, S, T};
-    __threadfence();
-    const uint32_t done = atomicAdd(counters + row, 1u);
-    sh.last = (done == static_cast<uint32_t>(nchunks - 1)) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!sh.last) return -1;
-  __threadfence();
-
-  const ChunkPartial* rp = partials + static_cast<int64_t>(row) * nchunks;
-  float rm = -INFINITY;
-  int ri = INT_MAX;
-  for (int c = threadIdx.x; c < nchunks; c += kThreads) {
-    const float cm = __ldcg(&rp[c].m);
-    const int ci = __ldcg(&rp[c].idx);
-    argmax_merge(rm, ri, cm, ci);
-  }
-  block_argmax(rm, ri, sh);
-  const float R2 = rm * kLog2e;
-  float RS = 0.f, RT = 0.f;
-  for (int c = threadIdx.x; c < nchunks; c += kThreads) {
-    const float cs = __ldcg(&rp[c].s);
-    if (cs > 0.f) {
-      const float delta = __ldcg(&rp[c].m) * kLog2e - R2;
-      const float f = ex2_approx(delta);
-      RS = fmaf(f, cs, RS);
-      RT = fmaf(f, fmaf(delta, cs, __ldcg(&rp[c].t)), RT);
-    }
-  }
-  block_sum2(RS, RT, sh);
-  if (threadIdx.x == 0) {
-    write_row(row, rm, ri, RS, RT, ids, entropy, log_conf);
-    counters[row] = 0u;  // ready for the next call
-  }
-  return row;
+  return Part{m, mi, S, T};
 }
 
+// Split path: one (row, chunk) per CTA; the last chunk of a row to finish merges the row.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) entropy_decode_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
+  constexpr int CE = chunk_elems<DT>();
   __shared__ BlockScratch sh;
+  __shared__ int last;
   pdl_wait();  // logits and row counts may come from the previous kernel in the stream
   pdl_launch_dependents();
-  entropy_chunk<DT>(blockIdx.x, a.logits, a.row_stride_bytes, a.V, a.nchunks, a.ids, a.entropy, a.log_conf,
-                    a.partials, a.counters, a.row_count, a.rows_per_group, sh);
+  const int64_t bid = blockIdx.x;
+  const int row = static_cast<int>(bid / a.nchunks);
+  const int chunk = static_cast<int>(bid - static_cast<int64_t>(row) * a.nchunks);
+  if (row_skipped(a, row)) return;
+  const char* rowp = a.logits + static_cast<int64_t>(row) * a.row_stride_bytes;
+  const int64_t c0 = static_cast<int64_t>(chunk) * CE;
+  const Part p = sub_chunk<DT, kSplitVec>(rowp, c0, min(static_cast<int64_t>(a.V), c0 + CE), sh);
+  if (a.nchunks == 1) {
+    if (threadIdx.x == 0) write_row(row, p.m, p.i, p.s, p.t, a.ids, a.entropy, a.log_conf);
+    return;
+  }
+  // Publish this chunk; the last chunk of the row to finish merges.
+  if (threadIdx.x == 0) {
+    a.partials[static_cast<int64_t>(row) * a.nchunks + chunk] = ChunkPartial{p.m, p.i, p.s, p.t};
+    __threadfence();
+    const uint32_t done = atomicAdd(a.counters + row, 1u);
+    last = (done == static_cast<uint32_t>(a.nchunks - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!last || threadIdx.x >= 32) return;
+  __threadfence();
+  const ChunkPartial* rp = a.partials + static_cast<int64_t>(row) * a.nchunks;
+  Part r{-INFINITY, INT_MAX, 0.f, 0.f};
+  for (int c = threadIdx.x; c < a.nchunks; c += 32)  // chunks in increasing order per lane
+    part_merge(r, Part{__ldcg(&rp[c].m), __ldcg(&rp[c].idx), __ldcg(&rp[c].s), __ldcg(&rp[c].t)});
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const Part o{__shfl_xor_sync(0xffffffffu, r.m, off), __shfl_xor_sync(0xffffffffu, r.i, off),
+                 __shfl_xor_sync(0xffffffffu, r.s, off), __shfl_xor_sync(0xffffffffu, r.t, off)};
+    part_merge(r, o);
+  }
+  if (threadIdx.x == 0) {
+    write_row(row, r.m, r.i, r.s, r.t, a.ids, a.entropy, a.log_conf);
+    a.counters[row] = 0u;  // ready for the next call
+  }
+}
+
+// Cluster path: one cluster per row; CTA `rank` of the cluster reduces its slice, the
+// cluster's first CTA merges the slices and writes the row result.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
+  constexpr int PV = Elem<DT>::kPerVec;
+  constexpr int64_t kSub = static_cast<int64_t>(kThreads) * kClusterVec * PV;  // elements per stretch
+  __shared__ BlockScratch sh;
+  __shared__ __align__(16) Part slice;
+  pdl_wait();  // logits and row counts may come from the previous kernel in the stream
+  pdl_launch_dependents();
+  const int csize = static_cast<int>(cluster_size());
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int row = static_cast<int>(cluster_id_x());
+  if (row_skipped(a, row)) return;  // the whole cluster skips the row
+  const char* rowp = a.logits + static_cast<int64_t>(row) * a.row_stride_bytes;
+  // slice of this CTA: whole vectors, the last slice takes the remainder (and the tail)
+  const int64_t nvec_row = (static_cast<int64_t>(a.V) + PV - 1) / PV;
+  const int64_t w = ((nvec_row + csize - 1) / csize) * PV;
+  const int64_t lo = min(static_cast<int64_t>(a.V), static_cast<int64_t>(rank) * w);
+  const int64_t hi = min(static_cast<int64_t>(a.V), lo + w);
+  // equal sub-chunks of at most kSub elements (whole vectors except the last)
+  const int64_t nsub = (hi - lo + kSub - 1) / kSub;
+  const int64_t step = nsub > 0 ? ((hi - lo + nsub - 1) / nsub + PV - 1) / PV * PV : 0;
+  Part acc{-INFINITY, INT_MAX, 0.f, 0.f};
+  for (int64_t c0 = lo; c0 < hi; c0 += step) {
+    const Part p = sub_chunk<DT, kClusterVec>(rowp, c0, min(hi, c0 + step), sh);
+    part_merge(acc, p);
+  }
+  if (threadIdx.x == 0) slice = acc;
+  cluster_sync_all();  // every slice result is in its CTA's shared memory
+  if (rank == 0 && threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    Part p{-INFINITY, INT_MAX, 0.f, 0.f};
+    if (lane < csize) {
+      const float4 q = dsmem_ld_f4(dsmem_map(smem_u32(&slice), static_cast<uint32_t>(lane)));
+      p = Part{q.x, __float_as_int(q.y), q.z, q.w};
+    }
+#pragma unroll
+    for (int off = 1; off < kMaxCluster; off <<= 1) {
+      const Part o{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.i, off),
+                   __shfl_xor_sync(0xffffffffu, p.s, off), __shfl_xor_sync(0xffffffffu, p.t, off)};
+      part_merge(p, o);
+    }
+    if (lane == 0) write_row(row, p.m, p.i, p.s, p.t, a.ids, a.entropy, a.log_conf);
+  }
+  cluster_sync_all();  // peers keep their shared memory until it has been read
 }
 
 }  // namespace
@@ -351,18 +427,33 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
                                   const int32_t* row_count, int32_t rows_per_group, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
+  const bool f32 = dtype == EC_F32;
+  const int per_vec = f32 ? Elem<EC_F32>::kPerVec : Elem<EC_BF16>::kPerVec;
+  const int64_t nvec = (static_cast<int64_t>(V) + per_vec - 1) / per_vec;
+  const int64_t per_cta = static_cast<int64_t>(kThreads) * kClusterVec;
+  const int csize = static_cast<int>(std::min<int64_t>(kMaxCluster, std::max<int64_t>(1, (nvec + per_cta - 1) / per_cta)));
   const int32_t nch = entropy_num_chunks(V, dtype);
   const size_t rows = static_cast<size_t>(n_rows);
-  auto* partials = static_cast<ChunkPartial*>(ws);
-  auto* counters = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) +
-                                               align_up(rows * nch * sizeof(ChunkPartial), 256));
+  EntArgs a{static_cast<const char*>(logits), row_stride * (f32 ? 4 : 2), V, nch, ids, entropy, log_conf,
+            static_cast<ChunkPartial*>(ws),
+            reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + align_up(rows * nch * sizeof(ChunkPartial), 256)),
+            row_count, rows_per_group};
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t cluster_ctas = static_cast<int64_t>(n_rows) * csize;
+  if (cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms || nch == 1 || ws == nullptr) {
+    if (cluster_ctas > INT_MAX) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(cluster_ctas));
+    if (f32) return launch_pdl_cluster(entropy_cluster_kernel<EC_F32>, grid, dim3(kThreads), 0, csize, s, a);
+    return launch_pdl_cluster(entropy_cluster_kernel<EC_BF16>, grid, dim3(kThreads), 0, csize, s, a);
+  }
   const int64_t nblocks = static_cast<int64_t>(n_rows) * nch;
   if (nblocks > INT_MAX) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(nblocks));
-  const EntArgs a{static_cast<const char*>(logits), row_stride * (dtype == EC_F32 ? 4 : 2), V, nch, ids, entropy,
-                  log_conf, partials, counters, row_count, rows_per_group};
-  if (dtype == EC_F32) return launch_pdl(entropy_decode_kernel<EC_F32>, grid, dim3(kThreads), 0, s, a);
-  return launch_pdl(entropy_decode_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, a);
+  if (f32) return launch_pdl(entropy_split_kernel<EC_F32>, grid, dim3(kThreads), 0, s, a);
+  return launch_pdl(entropy_split_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, a);
 }
 
 }  // namespace ec

@@ -35,10 +35,13 @@ def run_gpu(E, stored: np.ndarray, dtype: str, V: int):
     return ids.cpu().numpy(), ent.cpu().numpy().astype(np.float64), conf.cpu().numpy().astype(np.float64)
 
 
-def check(E, stored, dtype, V):
+def check(E, stored, dtype, V, reps=1):
+    """Oracle on the given rows; the kernel on the rows repeated `reps` times (many rows take
+    the kernel's one-CTA-per-chunk launch, few rows its one-cluster-per-row launch)."""
     x = O.widen(stored[:, :V], dtype)
     ids_o, ent_o, conf_o = O.entropy_decode(x)
-    ids, ent, conf = run_gpu(E, stored, dtype, V)
+    ids_o, ent_o, conf_o = np.tile(ids_o, reps), np.tile(ent_o, reps), np.tile(conf_o, reps)
+    ids, ent, conf = run_gpu(E, np.concatenate([stored] * reps) if reps > 1 else stored, dtype, V)
     np.testing.assert_array_equal(ids, ids_o)
     assert np.max(np.abs(ent - ent_o)) <= ENT_TOL, np.max(np.abs(ent - ent_o))
     assert np.max(np.abs(conf - conf_o)) <= ENT_TOL, np.max(np.abs(conf - conf_o))
@@ -63,11 +66,16 @@ def _bf16(a):
     return W.to_bf16_bits(np.asarray(a, dtype=np.float32))
 
 
-@pytest.mark.parametrize("V", [8192, 16384, 126464])
-def test_ties_across_chunk_boundaries(E, V):
+@pytest.mark.parametrize("reps", [1, 128])
+@pytest.mark.parametrize("V", [8192, 16384, 126464, 152064])
+def test_ties_across_chunk_boundaries(E, V, reps):
+    # maxima tied across the kernel's internal boundaries (8192-element chunks, slices of
+    # ceil(V / 8 / 8) * 8 elements) and at the row's ends; the lowest index must win
     rng = np.random.default_rng(V)
     rows = []
-    for pos in [(0, V - 1), (8191, 8192), (8192, 16383 if V > 16383 else V - 1), (V - 2, V - 1), (5, 8192 + 5)]:
+    sl = -(-V // 64) * 8
+    for pos in [(0, V - 1), (8191, 8192), (8192, 16383 if V > 16383 else V - 1), (V - 2, V - 1), (5, 8192 + 5),
+                (sl - 1, sl), (sl, 2 * sl + 3), (7 * sl - 1, V - 1)]:
         x = rng.standard_normal(V).astype(np.float32)
         for p in pos:
             if p < V:
@@ -76,19 +84,23 @@ def test_ties_across_chunk_boundaries(E, V):
     x = rng.standard_normal(V).astype(np.float32)
     x[:] = 3.0  # V-way tie
     rows.append(x)
+    x = rng.standard_normal(V).astype(np.float32)
+    x[997::997] = 30.0  # ties every 997 elements
+    rows.append(x)
     lg = _bf16(np.stack(rows))
-    check(E, lg, "bf16", V)
+    check(E, lg, "bf16", V, reps)
 
 
+@pytest.mark.parametrize("reps", [1, 128])
 @pytest.mark.parametrize("V,stride", [(50257, 50264), (1, 8), (7, 8), (8193, 8200), (32000, 32000)])
-def test_ragged_vocab_with_padded_stride(E, V, stride):
+def test_ragged_vocab_with_padded_stride(E, V, stride, reps):
     rng = np.random.default_rng(V)
     x = np.full((6, stride), 1e30, dtype=np.float32)  # padding must be ignored
     x[:, :V] = rng.standard_normal((6, V)) * np.array([0.5, 1, 2, 4, 8, 16])[:, None]
-    check(E, _bf16(x), "bf16", V)
+    check(E, _bf16(x), "bf16", V, reps)
     xf = np.full((6, stride), 1e30, dtype=np.float32)
     xf[:, :V] = x[:, :V]
-    check(E, xf, "f32", V)
+    check(E, xf, "f32", V, reps)
 
 
 def test_neg_inf_one_hot_and_uniform_fp32(E):

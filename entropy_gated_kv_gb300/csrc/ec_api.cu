@@ -136,7 +136,7 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
   if (entropy_num_chunks(V, dtype) > 1 && (ws == nullptr || ws_bytes < need || !aligned16(ws)))
     return EC_ERR_INVALID_ARG;
   return cuda_status(launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf, ws,
-                                           nullptr, 1, static_cast<cudaStream_t>(stream)));
+                                           nullptr, 1, true, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- (b)+(c) --------------------------------------------------------------------------------
@@ -223,7 +223,7 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
 
   // stages (a)-(c): decode + entropy of the candidate rows, then the select stage
   cudaError_t e = launch_entropy_decode(logits, p->V, p->B * p->C_max, p->V, p->logits_dtype, ids, ent, conf,
-                                        w + lay.k1, cand_count, p->C_max, s);
+                                        w + lay.k1, cand_count, p->C_max, false, s);
   if (e == cudaSuccess) e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, s);
   if (e != cudaSuccess) return EC_ERR_CUDA;
   for (int32_t l = 0; l < n_layers; ++l) {

@@ -24,10 +24,14 @@ int entropy_chunk_elems(int32_t dtype);
 int32_t entropy_num_chunks(int32_t V, int32_t dtype);
 size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype);
 // row_count (may be null): rows r with (r % rows_per_group) >= row_count[r / rows_per_group]
-// are skipped (their outputs are left untouched).
+// are skipped (their outputs are left untouched). allow_cluster: few rows may take the
+// one-cluster-per-row launch (lowest latency on an idle GPU); without it, or with many rows,
+// the one-CTA-per-chunk launch runs, whose small independent CTAs become resident while a
+// large predecessor kernel is still running (the better choice inside a chain of kernels).
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
-                                  const int32_t* row_count, int32_t rows_per_group, cudaStream_t s);
+                                  const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
+                                  cudaStream_t s);
 
 // ---- select_recompute ---------------------------------------------------------------------
 struct SelArgs;

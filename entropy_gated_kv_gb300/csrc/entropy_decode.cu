@@ -16,7 +16,8 @@
 //     Stretches combine by rescaling S and T to the larger max (part_merge).
 //     H = ln2 (log2 S - T/S). Each thread issues all its 16-byte streaming loads of a
 //     stretch before any arithmetic.
-//   - Few rows (the whole problem within about one wave): one thread-block cluster of up to
+//   - Few rows (the whole problem within about one wave), when the caller allows it (the
+//     standalone entry; not the chained step, see launch_entropy_decode): one cluster of up to
 //     8 CTAs per row, CTA r owning a contiguous slice of the row; the slices merge on chip:
 //     each CTA leaves its (max, index, S, T) in shared memory and, after one cluster barrier,
 //     the first CTA reads them through distributed shared memory and writes the row result.
@@ -425,7 +426,8 @@ size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype) {
 
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
-                                  const int32_t* row_count, int32_t rows_per_group, cudaStream_t s) {
+                                  const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
+                                  cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const bool f32 = dtype == EC_F32;
   const int per_vec = f32 ? Elem<EC_F32>::kPerVec : Elem<EC_BF16>::kPerVec;
@@ -443,7 +445,8 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t cluster_ctas = static_cast<int64_t>(n_rows) * csize;
-  if (cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms || nch == 1 || ws == nullptr) {
+  if ((allow_cluster && cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms) || nch == 1 ||
+      ws == nullptr) {
     if (cluster_ctas > INT_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(cluster_ctas));
     if (f32) return launch_pdl_cluster(entropy_cluster_kernel<EC_F32>, grid, dim3(kThreads), 0, csize, s, a);

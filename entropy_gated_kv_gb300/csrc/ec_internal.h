@@ -36,11 +36,12 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
 // ---- select_recompute ---------------------------------------------------------------------
 struct SelArgs;
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
-                      const int32_t* ids, const float* entropy, const float* log_conf);
+                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early);
 size_t select_smem_bytes(const ec_params& p);
+// prefetch_early: stage the decode state before the grid dependency wait (see SelArgs).
 cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
                                     const int32_t* cand_count, const int32_t* ids, const float* entropy,
-                                    const float* log_conf, cudaStream_t s);
+                                    const float* log_conf, bool prefetch_early, cudaStream_t s);
 
 // ---- kv_scatter (+ optional query gather) -------------------------------------------------
 cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, const void* k_new,

@@ -41,6 +41,10 @@ struct SelArgs {
   int32_t* idx;
   int32_t* R;
   int32_t* dev_err;
+  // Stage the decode state before waiting on the previous kernel: only when every kernel that
+  // writes the state (mask, ring, candidates) has completed before this launch's predecessor
+  // released it (inside a step, where the predecessor is the decode kernel).
+  int32_t prefetch_early;
 };
 
 constexpr int kSelMaxRingSmem = 4096;  // histories up to this length are staged in smem
@@ -49,6 +53,7 @@ struct SelHdr {
   int warp_tmp[32];
   float warp_e[32];
   int warp_nan[32];
+  int word_off[32];  // fast path: idx offset of each bitmap word (words <= 32)
   int head, count, full, carry;
 };
 
@@ -138,29 +143,6 @@ __device__ __forceinline__ uint32_t sel_bytes_to_bits(uint4 lo, uint4 hi) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) bits |= (((w[q] >> (8 * e)) & 0xFFu) != 0u ? 1u : 0u) << (4 * q + e);
   return bits;
-}
-
-// Warp-wide: the set bits of words [0, nwords) written to idx in ascending order; returns
-// the count (nwords <= 32). Lane w computes the prefix count of word w; then, word by word,
-// lane j writes bit j — independent iterations, no lane loops over its own bits.
-__device__ __forceinline__ int sel_warp_compact(const uint32_t* bitmap, int nwords, int32_t* idx_row, int lane) {
-  const uint32_t mine = lane < nwords ? bitmap[lane] : 0u;
-  const int c = __popc(mine);
-  int incl = c;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += t;
-  }
-  const int excl = incl - c;
-  const uint32_t below = (1u << lane) - 1u;
-#pragma unroll 8
-  for (int w = 0; w < nwords; ++w) {
-    const uint32_t word = __shfl_sync(0xffffffffu, mine, w);
-    const int base = __shfl_sync(0xffffffffu, excl, w);
-    if ((word >> lane) & 1u) idx_row[base + __popc(word & below)] = (w << 5) + lane;
-  }
-  return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 // Warp argmax over (confidence, -position): the best-ranked lane among `live`, or -1.
@@ -343,9 +325,17 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
           else report_error(a.dev_err, EC_DEVERR_BAD_IDX);
         }
         __syncwarp();
-        if (nwords <= 32) {
-          const int R = sel_warp_compact(bitmap, nwords, a.idx + rowL, lane);
-          if (lane == 0) a.R[b] = R;
+        if (nwords <= 32) {  // offsets of each word's bits in idx; every warp writes below
+          const uint32_t mine = lane < nwords ? bitmap[lane] : 0u;
+          const int c = __popc(mine);
+          int incl = c;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+          }
+          h.word_off[lane] = incl - c;
+          if (lane == 31) a.R[b] = incl;
         }
       }
     }
@@ -441,7 +431,14 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
     if (tid == 0) a.R[b] = L;
     return;
   }
-  if (fast && nwords <= 32) return;  // warp 0 has compacted already
+  if (fast && nwords <= 32) {
+    // word w of the bitmap goes to idx[word_off[w] ...]: lane j of a warp writes bit j
+    for (int w = warp; w < nwords; w += W) {
+      const uint32_t word = bitmap[w];
+      if ((word >> lane) & 1u) a.idx[rowL + h.word_off[w] + __popc(word & ((1u << lane) - 1u))] = (w << 5) + lane;
+    }
+    return;
+  }
   for (int base = 0; base < nwords; base += NT) {
     const int w = base + tid;
     const uint32_t bits = (w < nwords) ? bitmap[w] : 0u;
@@ -463,13 +460,3 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
 
 }  // namespace ec
 
-namespace ec {
-
-// Stages (b)+(c) for sequence b in one go (prefetch, then finish).
-template <int NT>
-__device__ void select_sequence(const SelArgs& a, int b, uint8_t* dyn) {
-  select_prefetch<NT>(a, b, dyn);
-  select_finish<NT>(a, b, dyn);
-}
-
-}  // namespace ec

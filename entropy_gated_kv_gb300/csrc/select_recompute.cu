@@ -1,6 +1,6 @@
 // select_recompute.cu — stages (b) and (c) of the EntropyCache step as a kernel of their own
-// (ec_select_recompute, and inside ec_step): one CTA per sequence runs select_sequence
-// (select_device.cuh).
+// (ec_select_recompute, and inside ec_step): one CTA per sequence runs select_prefetch and
+// select_finish (select_device.cuh).
 #include "ec_internal.h"
 #include "select_device.cuh"
 
@@ -11,16 +11,24 @@ constexpr int kThreads = 512;
 
 __global__ void __launch_bounds__(kThreads) select_recompute_kernel(SelArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
-  pdl_wait();  // decode results and state may come from the previous kernels in the stream
-  pdl_launch_dependents();
-  select_sequence<kThreads>(a, blockIdx.x, dyn);
+  if (a.prefetch_early) {
+    select_prefetch<kThreads>(a, blockIdx.x, dyn);
+    pdl_wait();  // the decode results come from the previous kernel
+    pdl_launch_dependents();
+  } else {
+    pdl_wait();  // decode results and state may come from the previous kernels in the stream
+    pdl_launch_dependents();
+    select_prefetch<kThreads>(a, blockIdx.x, dyn);
+  }
+  select_finish<kThreads>(a, blockIdx.x, dyn);
 }
 
 }  // namespace
 
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
-                      const int32_t* ids, const float* entropy, const float* log_conf) {
+                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early) {
   SelArgs a;
+  a.prefetch_early = prefetch_early ? 1 : 0;
   a.L = p.L;
   a.C_max = p.C_max;
   a.k = p.k;
@@ -49,7 +57,7 @@ size_t select_smem_bytes(const ec_params& p) { return static_cast<size_t>(sel_la
 
 cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
                                     const int32_t* cand_count, const int32_t* ids, const float* entropy,
-                                    const float* log_conf, cudaStream_t s) {
+                                    const float* log_conf, bool prefetch_early, cudaStream_t s) {
   const size_t smem = select_smem_bytes(p);
   static size_t configured = 48 * 1024;
   if (smem > configured) {
@@ -59,7 +67,7 @@ cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, cons
     configured = smem;
   }
   return launch_pdl(select_recompute_kernel, dim3(p.B), dim3(kThreads), smem, s,
-                    make_sel_args(p, st, cand_pos, cand_count, ids, entropy, log_conf));
+                    make_sel_args(p, st, cand_pos, cand_count, ids, entropy, log_conf, prefetch_early));
 }
 
 }  // namespace ec

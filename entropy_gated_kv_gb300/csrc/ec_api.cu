@@ -136,7 +136,7 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
   if (entropy_num_chunks(V, dtype) > 1 && (ws == nullptr || ws_bytes < need || !aligned16(ws)))
     return EC_ERR_INVALID_ARG;
   return cuda_status(launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf, ws,
-                                           nullptr, 1, true, static_cast<cudaStream_t>(stream)));
+                                           nullptr, 1, true, false, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- (b)+(c) --------------------------------------------------------------------------------
@@ -147,8 +147,8 @@ ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int3
   if (r != EC_OK) return r;
   if ((r = check_state(st)) != EC_OK) return r;
   if (!cand_pos || !cand_count || !ids || !entropy || !log_conf) return EC_ERR_INVALID_ARG;
-  return cuda_status(launch_select_recompute(*p, *st, cand_pos, cand_count, ids, entropy, log_conf, false,
-                                             static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_select_recompute(*p, *st, cand_pos, cand_count, ids, entropy, log_conf, false, nullptr,
+                                             0, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- (c) scatter ------------------------------------------------------------------------------
@@ -223,10 +223,13 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
 
   // stages (a)-(c): decode + entropy of the candidate rows, then the select stage
   cudaError_t e = launch_entropy_decode(logits, p->V, p->B * p->C_max, p->V, p->logits_dtype, ids, ent, conf,
-                                        w + lay.k1, cand_count, p->C_max, false, s);
+                                        w + lay.k1, cand_count, p->C_max, false, true, s);
   // the decode kernel waits for every earlier kernel before it releases this one, so the select
   // kernel may stage the state before its own wait
-  if (e == cudaSuccess) e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, true, s);
+  if (e == cudaSuccess)
+    e = launch_select_recompute(*p, *st, cand_pos, cand_count, ids, ent, conf, true,
+                                reinterpret_cast<const ChunkPartial*>(w + lay.k1), entropy_num_chunks(p->V, p->logits_dtype),
+                                s);
   if (e != cudaSuccess) return EC_ERR_CUDA;
   for (int32_t l = 0; l < n_layers; ++l) {
     e = launch_kv_scatter(*p, k_cache[l], v_cache[l], k_src[l], v_src[l], 1, st->idx, st->R, q_src[l],

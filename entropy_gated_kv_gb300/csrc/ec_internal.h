@@ -28,20 +28,27 @@ size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype);
 // one-cluster-per-row launch (lowest latency on an idle GPU); without it, or with many rows,
 // the one-CTA-per-chunk launch runs, whose small independent CTAs become resident while a
 // large predecessor kernel is still running (the better choice inside a chain of kernels).
+// publish_only: the one-CTA-per-chunk launch writes each chunk's (max, index, S, T) to the
+// workspace partials and stops; the next kernel merges them (ids / entropy / log_conf are not
+// written).
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
                                   const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
-                                  cudaStream_t s);
+                                  bool publish_only, cudaStream_t s);
 
 // ---- select_recompute ---------------------------------------------------------------------
 struct SelArgs;
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
-                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early);
+                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early,
+                      const ChunkPartial* partials, int32_t nchunks);
 size_t select_smem_bytes(const ec_params& p);
-// prefetch_early: stage the decode state before the grid dependency wait (see SelArgs).
+// prefetch_early: stage the decode state before the grid dependency wait; partials (may be
+// null): merge the decode kernel's per-chunk partials instead of reading ids / entropy /
+// log_conf (see SelArgs).
 cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
                                     const int32_t* cand_count, const int32_t* ids, const float* entropy,
-                                    const float* log_conf, bool prefetch_early, cudaStream_t s);
+                                    const float* log_conf, bool prefetch_early, const ChunkPartial* partials,
+                                    int32_t nchunks, cudaStream_t s);
 
 // ---- kv_scatter (+ optional query gather) -------------------------------------------------
 cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, const void* k_new,

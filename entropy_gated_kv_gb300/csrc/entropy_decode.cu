@@ -13,7 +13,7 @@
 //   - Two passes over registers per stretch: (1) max and lowest index over the raw stored
 //     values (exact, no rescaling before comparison), block-reduced; (2) S = sum 2^d and
 //     T = sum d 2^d with d = (x - M) log2(e) relative to the stretch max M, block-reduced.
-//     Stretches combine by rescaling S and T to the larger max (part_merge).
+//     Stretches combine by rescaling S and T to the larger max (entropy_merge.cuh).
 //     H = ln2 (log2 S - T/S). Each thread issues all its 16-byte streaming loads of a
 //     stretch before any arithmetic.
 //   - Few rows (the whole problem within about one wave), when the caller allows it (the
@@ -31,6 +31,7 @@
 
 #include "ec_common.cuh"
 #include "ec_internal.h"
+#include "entropy_merge.cuh"
 
 namespace ec {
 namespace {
@@ -42,7 +43,6 @@ constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
 constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs
 constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 template <int DT>
 struct Elem;
@@ -99,20 +99,12 @@ __device__ __forceinline__ float load_one(const char* row, int64_t j) {
   }
 }
 
-// Larger value wins; equal values: lower index wins.
-__device__ __forceinline__ void argmax_merge(float& m, int& i, float m2, int i2) {
-  if (m2 > m || (m2 == m && i2 < i)) {
-    m = m2;
-    i = i2;
-  }
-}
-
 __device__ __forceinline__ void warp_argmax(float& m, int& i) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
-    argmax_merge(m, i, m2, i2);
+    ent_argmax_merge(m, i, m2, i2);
   }
 }
 
@@ -180,13 +172,11 @@ __device__ __forceinline__ void block_sum2(float& a, float& b, BlockScratch& sh)
   b = sh.bt;
 }
 
-__device__ __forceinline__ void write_row(int row, float m_unused, int idx, float S, float T, int32_t* ids,
-                                          float* entropy, float* log_conf) {
-  (void)m_unused;
-  const float l2s = lg2_approx(S);
-  ids[row] = idx;
-  entropy[row] = kLn2 * (l2s - T / S);
-  log_conf[row] = -kLn2 * l2s;
+using Part = EntPart;
+
+__device__ __forceinline__ void write_row(int row, const Part& p, int32_t* ids, float* entropy, float* log_conf) {
+  ids[row] = p.i;
+  ent_finish(p, entropy[row], log_conf[row]);
 }
 
 struct EntArgs {
@@ -198,6 +188,7 @@ struct EntArgs {
   float* log_conf;
   ChunkPartial* partials;  // split path only
   uint32_t* counters;      // split path only
+  int32_t publish_only;    // split path: write each chunk's partial and stop (the reader merges)
   const int32_t* row_count;
   int32_t rows_per_group;
 };
@@ -207,36 +198,6 @@ __device__ __forceinline__ bool row_skipped(const EntArgs& a, int row) {
   if (a.row_count == nullptr) return false;
   const int grp = row / a.rows_per_group;
   return row - grp * a.rows_per_group >= __ldg(a.row_count + grp);
-}
-
-// (max, index, S, T) of a stretch of one row, S and T relative to its own max (log2 units).
-struct Part {
-  float m;
-  int i;
-  float s;
-  float t;
-};
-
-// Adds stretch b to stretch a: argmax with the lower-index rule (also over stretches whose
-// values are all -inf), S and T rescaled to the larger max. S >= 1 whenever a stretch's max
-// is finite (its maximum contributes 2^0), so S == 0 marks a stretch without mass.
-__device__ __forceinline__ void part_merge(Part& a, const Part& b) {
-  float m = a.m;
-  int i = a.i;
-  argmax_merge(m, i, b.m, b.i);
-  if (b.s > 0.f) {
-    if (a.s > 0.f) {
-      const float da = (a.m - m) * kLog2e, db = (b.m - m) * kLog2e;
-      const float fa = ex2_approx(da), fb = ex2_approx(db);
-      a.t = fa * fmaf(da, a.s, a.t) + fb * fmaf(db, b.s, b.t);
-      a.s = fa * a.s + fb * b.s;
-    } else {
-      a.s = b.s;
-      a.t = b.t;
-    }
-  }
-  a.m = m;
-  a.i = i;
 }
 
 // One stretch [c0, c1) of a row (c0 a multiple of the vector width, at most NV vectors per
@@ -329,8 +290,12 @@ __global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
   const char* rowp = a.logits + static_cast<int64_t>(row) * a.row_stride_bytes;
   const int64_t c0 = static_cast<int64_t>(chunk) * CE;
   const Part p = sub_chunk<DT, kSplitVec>(rowp, c0, min(static_cast<int64_t>(a.V), c0 + CE), sh);
+  if (a.publish_only) {  // the step's select kernel merges the chunks of each row itself
+    if (threadIdx.x == 0) a.partials[static_cast<int64_t>(row) * a.nchunks + chunk] = ChunkPartial{p.m, p.i, p.s, p.t};
+    return;
+  }
   if (a.nchunks == 1) {
-    if (threadIdx.x == 0) write_row(row, p.m, p.i, p.s, p.t, a.ids, a.entropy, a.log_conf);
+    if (threadIdx.x == 0) write_row(row, p, a.ids, a.entropy, a.log_conf);
     return;
   }
   // Publish this chunk; the last chunk of the row to finish merges.
@@ -346,15 +311,10 @@ __global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
   const ChunkPartial* rp = a.partials + static_cast<int64_t>(row) * a.nchunks;
   Part r{-INFINITY, INT_MAX, 0.f, 0.f};
   for (int c = threadIdx.x; c < a.nchunks; c += 32)  // chunks in increasing order per lane
-    part_merge(r, Part{__ldcg(&rp[c].m), __ldcg(&rp[c].idx), __ldcg(&rp[c].s), __ldcg(&rp[c].t)});
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const Part o{__shfl_xor_sync(0xffffffffu, r.m, off), __shfl_xor_sync(0xffffffffu, r.i, off),
-                 __shfl_xor_sync(0xffffffffu, r.s, off), __shfl_xor_sync(0xffffffffu, r.t, off)};
-    part_merge(r, o);
-  }
+    ent_part_merge(r, Part{__ldcg(&rp[c].m), __ldcg(&rp[c].idx), __ldcg(&rp[c].s), __ldcg(&rp[c].t)});
+  r = ent_warp_merge(r);
   if (threadIdx.x == 0) {
-    write_row(row, r.m, r.i, r.s, r.t, a.ids, a.entropy, a.log_conf);
+    write_row(row, r, a.ids, a.entropy, a.log_conf);
     a.counters[row] = 0u;  // ready for the next call
   }
 }
@@ -385,7 +345,7 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
   Part acc{-INFINITY, INT_MAX, 0.f, 0.f};
   for (int64_t c0 = lo; c0 < hi; c0 += step) {
     const Part p = sub_chunk<DT, kClusterVec>(rowp, c0, min(hi, c0 + step), sh);
-    part_merge(acc, p);
+    ent_part_merge(acc, p);
   }
   if (threadIdx.x == 0) slice = acc;
   cluster_sync_all();  // every slice result is in its CTA's shared memory
@@ -400,9 +360,9 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
     for (int off = 1; off < kMaxCluster; off <<= 1) {
       const Part o{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.i, off),
                    __shfl_xor_sync(0xffffffffu, p.s, off), __shfl_xor_sync(0xffffffffu, p.t, off)};
-      part_merge(p, o);
+      ent_part_merge(p, o);
     }
-    if (lane == 0) write_row(row, p.m, p.i, p.s, p.t, a.ids, a.entropy, a.log_conf);
+    if (lane == 0) write_row(row, p, a.ids, a.entropy, a.log_conf);
   }
   cluster_sync_all();  // peers keep their shared memory until it has been read
 }
@@ -427,7 +387,7 @@ size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype) {
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
                                   const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
-                                  cudaStream_t s) {
+                                  bool publish_only, cudaStream_t s) {
   if (n_rows == 0) return cudaSuccess;
   const bool f32 = dtype == EC_F32;
   const int per_vec = f32 ? Elem<EC_F32>::kPerVec : Elem<EC_BF16>::kPerVec;
@@ -439,14 +399,14 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   EntArgs a{static_cast<const char*>(logits), row_stride * (f32 ? 4 : 2), V, nch, ids, entropy, log_conf,
             static_cast<ChunkPartial*>(ws),
             reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + align_up(rows * nch * sizeof(ChunkPartial), 256)),
-            row_count, rows_per_group};
+            publish_only ? 1 : 0, row_count, rows_per_group};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t cluster_ctas = static_cast<int64_t>(n_rows) * csize;
-  if ((allow_cluster && cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms) || nch == 1 ||
-      ws == nullptr) {
+  if (!publish_only &&
+      ((allow_cluster && cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms) || nch == 1 || ws == nullptr)) {
     if (cluster_ctas > INT_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(cluster_ctas));
     if (f32) return launch_pdl_cluster(entropy_cluster_kernel<EC_F32>, grid, dim3(kThreads), 0, csize, s, a);

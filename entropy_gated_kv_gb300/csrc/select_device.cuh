@@ -19,6 +19,8 @@
 #include <cmath>
 
 #include "ec_common.cuh"
+#include "ec_internal.h"
+#include "entropy_merge.cuh"
 
 namespace ec {
 
@@ -45,7 +47,12 @@ struct SelArgs {
   // writes the state (mask, ring, candidates) has completed before this launch's predecessor
   // released it (inside a step, where the predecessor is the decode kernel).
   int32_t prefetch_early;
+  // Inside a step: the decode kernel's per-chunk partials ([B * C_max][nchunks]), merged here
+  // instead of reading ids / entropy / log_conf (null: read those).
+  const ChunkPartial* partials;
+  int32_t nchunks;
 };
+static_assert(sizeof(ChunkPartial) == 16, "partials are read as one 16-byte vector");
 
 constexpr int kSelMaxRingSmem = 4096;  // histories up to this length are staged in smem
 
@@ -246,12 +253,37 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
     if (tid == 0) report_error(a.dev_err, EC_DEVERR_BAD_R);
     count = min(max(count, 0), C_max);
   }
-  for (int i = tid; i < C_max; i += NT) {
-    float c = __ldcg(a.log_conf + rowC + i);
-    if (isnan(c)) c = -INFINITY;  // NaN confidence ranks lowest
-    s_conf[i] = c;
-    s_ent[i] = __ldcg(a.entropy + rowC + i);
-    s_id[i] = __ldcg(a.ids + rowC + i);
+  if (a.partials != nullptr) {
+    // merge each candidate row's chunks: 16 lanes per row (two rows per warp, all rows of one
+    // pass in flight at once), lane k of a group taking chunks k, k + 16, ...
+    const int grp = lane >> 4, gl = lane & 15;
+    for (int i0 = 2 * warp; i0 < C_max; i0 += 2 * W) {
+      const int i = i0 + grp;
+      EntPart pt{-INFINITY, INT_MAX, 0.f, 0.f};
+      if (i < count) {  // rows past the count were skipped by the decode kernel
+        const float4* rp = reinterpret_cast<const float4*>(a.partials + (rowC + i) * a.nchunks);
+        for (int c = gl; c < a.nchunks; c += 16) {
+          const float4 q = __ldcg(rp + c);
+          ent_part_merge(pt, EntPart{q.x, __float_as_int(q.y), q.z, q.w});
+        }
+      }
+      pt = ent_group16_merge(pt);
+      if (gl == 0 && i < C_max) {
+        float h, c;
+        ent_finish(pt, h, c);
+        s_conf[i] = isnan(c) ? -INFINITY : c;  // NaN confidence ranks lowest
+        s_ent[i] = h;
+        s_id[i] = pt.i;
+      }
+    }
+  } else {
+    for (int i = tid; i < C_max; i += NT) {
+      float c = __ldcg(a.log_conf + rowC + i);
+      if (isnan(c)) c = -INFINITY;  // NaN confidence ranks lowest
+      s_conf[i] = c;
+      s_ent[i] = __ldcg(a.entropy + rowC + i);
+      s_id[i] = __ldcg(a.ids + rowC + i);
+    }
   }
   __syncthreads();
 

@@ -26,9 +26,12 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(SelArgs a) {
 }  // namespace
 
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
-                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early) {
+                      const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early,
+                      const ChunkPartial* partials, int32_t nchunks) {
   SelArgs a;
   a.prefetch_early = prefetch_early ? 1 : 0;
+  a.partials = partials;
+  a.nchunks = nchunks;
   a.L = p.L;
   a.C_max = p.C_max;
   a.k = p.k;
@@ -57,7 +60,8 @@ size_t select_smem_bytes(const ec_params& p) { return static_cast<size_t>(sel_la
 
 cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, const int32_t* cand_pos,
                                     const int32_t* cand_count, const int32_t* ids, const float* entropy,
-                                    const float* log_conf, bool prefetch_early, cudaStream_t s) {
+                                    const float* log_conf, bool prefetch_early, const ChunkPartial* partials,
+                                    int32_t nchunks, cudaStream_t s) {
   const size_t smem = select_smem_bytes(p);
   static size_t configured = 48 * 1024;
   if (smem > configured) {
@@ -67,7 +71,8 @@ cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, cons
     configured = smem;
   }
   return launch_pdl(select_recompute_kernel, dim3(p.B), dim3(kThreads), smem, s,
-                    make_sel_args(p, st, cand_pos, cand_count, ids, entropy, log_conf, prefetch_early));
+                    make_sel_args(p, st, cand_pos, cand_count, ids, entropy, log_conf, prefetch_early, partials,
+                                  nchunks));
 }
 
 }  // namespace ec

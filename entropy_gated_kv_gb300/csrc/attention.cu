@@ -169,20 +169,22 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Hq, int Hkv, int g,
     int nr, float scale_log2, uint16_t* __restrict__ out, int32_t* __restrict__ dev_err) {
   using LY = Layout<D>;
-  constexpr int kRedStride = D + 4;  // fp32 row stride of the staged partial (16-byte padded)
+  // A staged partial row: O as D bf16 (unnormalised; one more rounding than the fp32
+  // accumulator, far below the output's own bf16 rounding after the merge), then the running
+  // max and running sum as fp32, padded to 16 bytes.
+  constexpr int kRowBytes = 2 * D + 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + LY::kBarOff);
   uint8_t* q_smem = smem + LY::kQOff;
-  // Split partials reuse the K/V stages and P buffers once every CTA of the cluster is past
-  // its compute: `send` holds this CTA's 128 partial rows (D values, then the running max and
-  // running sum in the row's padding), grouped by the peer that merges them; `recv` holds
-  // the kBlockM / kCluster rows this CTA merges, one slice per peer.
+  // Split partials reuse the K/V stages once every CTA of the cluster is past its compute:
+  // `send` holds this CTA's 128 partial rows, grouped by the peer that merges them; `recv`
+  // holds the kBlockM / kCluster rows this CTA merges, one slice per peer.
   constexpr int kSliceRows = kBlockM / kCluster;
-  constexpr uint32_t kSliceBytes = kSliceRows * kRedStride * 4;
-  float* send = reinterpret_cast<float*>(smem + LY::kStageOff);
-  float* recv = send + kBlockM * kRedStride;
-  static_assert(LY::kStageOff + 2 * kBlockM * kRedStride * 4 <= LY::kBarOff, "split buffers overlap barriers");
+  constexpr uint32_t kSliceBytes = kSliceRows * kRowBytes;
+  uint8_t* send = smem + LY::kStageOff;
+  uint8_t* recv = send + kBlockM * kRowBytes;
+  static_assert(LY::kStageOff + 2 * kBlockM * kRowBytes <= LY::kBarOff, "split buffers overlap barriers");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M_rows = nr * g;
   const int cluster = static_cast<int>(cluster_id_x());
@@ -435,28 +437,30 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       } else {
         // One split of a shared tile: stage the unnormalised partial for the cluster merge.
         // Every K/V load of this CTA has been consumed (o_full), so the stages are free.
-        float* ro = send + row * kRedStride;
+        uint8_t* ro = send + row * kRowBytes;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
           EC_TMEM_LD32(tmem + lane_off + kTmemO + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(ro + c * 32 + 4 * q) =
-                make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]), __uint_as_float(o[4 * q + 2]),
-                            __uint_as_float(o[4 * q + 3]));
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(ro + 2 * (c * 32 + 8 * q)) =
+                make_uint4(pack_bf16x2(__uint_as_float(o[8 * q + 0]), __uint_as_float(o[8 * q + 1])),
+                           pack_bf16x2(__uint_as_float(o[8 * q + 2]), __uint_as_float(o[8 * q + 3])),
+                           pack_bf16x2(__uint_as_float(o[8 * q + 4]), __uint_as_float(o[8 * q + 5])),
+                           pack_bf16x2(__uint_as_float(o[8 * q + 6]), __uint_as_float(o[8 * q + 7])));
         }
-        ro[D] = m_used;
-        ro[D + 1] = l_sum;
+        reinterpret_cast<float*>(ro + 2 * D)[0] = m_used;
+        reinterpret_cast<float*>(ro + 2 * D)[1] = l_sum;
         staged = true;
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free);
     }
     if (split_mode && !staged) {  // no split of its own (or a failed one): contribute nothing
-      send[row * kRedStride + D] = -INFINITY;
-      send[row * kRedStride + D + 1] = 0.f;
+      reinterpret_cast<float*>(send + row * kRowBytes + 2 * D)[0] = -INFINITY;
+      reinterpret_cast<float*>(send + row * kRowBytes + 2 * D)[1] = 0.f;
     }
     if (split_mode) fence_proxy_async_smem();  // the bulk copies below read `send`
   }
@@ -469,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       // push each peer the slice of rows it merges (the own slice stays in `send`)
       for (int d = 1; d < kCluster; ++d) {
         const uint32_t dst = (rank + d) % kCluster;
-        const uint32_t dst_recv = dsmem_map(smem_u32(recv + rank * kSliceRows * kRedStride), dst);
-        bulk_copy_s2cluster(dst_recv, send + dst * kSliceRows * kRedStride, kSliceBytes,
+        const uint32_t dst_recv = dsmem_map(smem_u32(recv + rank * kSliceBytes), dst);
+        bulk_copy_s2cluster(dst_recv, send + dst * kSliceBytes, kSliceBytes,
                             dsmem_map(smem_u32(&bars->recv), dst));
       }
     }
@@ -484,16 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
         const int srow = t >> 2;  // row within this CTA's slice
         const int prow = rank * kSliceRows + srow;
         const int col0 = (t & 3) * kCols;
-        const float* src[kCluster];
+        const uint8_t* src[kCluster];
 #pragma unroll
         for (int sidx = 0; sidx < kCluster; ++sidx)
-          src[sidx] = (sidx == rank) ? send + prow * kRedStride : recv + (sidx * kSliceRows + srow) * kRedStride;
+          src[sidx] = (sidx == rank) ? send + prow * kRowBytes : recv + (sidx * kSliceRows + srow) * kRowBytes;
         float wgt[kCluster], ls[kCluster];
         float mmax = -INFINITY;
 #pragma unroll
         for (int sidx = 0; sidx < kCluster; ++sidx) {
-          wgt[sidx] = src[sidx][D];
-          ls[sidx] = src[sidx][D + 1];
+          wgt[sidx] = reinterpret_cast<const float*>(src[sidx] + 2 * D)[0];
+          ls[sidx] = reinterpret_cast<const float*>(src[sidx] + 2 * D)[1];
           if (ls[sidx] > 0.f) mmax = fmaxf(mmax, wgt[sidx]);
         }
         float lsum = 0.f;
@@ -509,14 +513,16 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
 #pragma unroll
         for (int sidx = 0; sidx < kCluster; ++sidx) {
           if (wgt[sidx] == 0.f) continue;  // an empty split may hold stale values
-          const float4* o4 = reinterpret_cast<const float4*>(src[sidx] + col0);
+          const uint4* o8 = reinterpret_cast<const uint4*>(src[sidx] + 2 * col0);
 #pragma unroll
-          for (int q = 0; q < kCols / 4; ++q) {
-            const float4 v = o4[q];
-            acc[4 * q + 0] = fmaf(wgt[sidx], v.x, acc[4 * q + 0]);
-            acc[4 * q + 1] = fmaf(wgt[sidx], v.y, acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(wgt[sidx], v.z, acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(wgt[sidx], v.w, acc[4 * q + 3]);
+          for (int q = 0; q < kCols / 8; ++q) {
+            const uint4 v = o8[q];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc[8 * q + 2 * e] = fmaf(wgt[sidx], bf16lo_to_f32(w[e]), acc[8 * q + 2 * e]);
+              acc[8 * q + 2 * e + 1] = fmaf(wgt[sidx], bf16hi_to_f32(w[e]), acc[8 * q + 2 * e + 1]);
+            }
           }
         }
         const int rl = prow / g, jh = prow - rl * g;

@@ -102,7 +102,7 @@ __device__ __forceinline__ int warp_sum(int v) {
 __device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int nclusters) {
   const int lane = threadIdx.x & 31;
   int t = 0;
-  for (int b = lane; b < B; b += 32) t += Hkv * ((clamp_r(__ldg(R + b), L) + nr - 1) / nr);
+  for (int b = lane; b < B; b += 32) t += Hkv * ((clamp_r(__ldcg(R + b), L) + nr - 1) / nr);
   t = warp_sum(t);
   Plan p;
   p.tiles = t;
@@ -131,7 +131,7 @@ __device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, i
   int base = 0;
   for (int b0 = 0; b0 < B; b0 += 32) {
     const int b = b0 + lane;
-    const int rb = b < B ? clamp_r(__ldg(R + b), L) : 0;
+    const int rb = b < B ? clamp_r(__ldcg(R + b), L) : 0;
     const int tb = b < B ? Hkv * ((rb + nr - 1) / nr) : 0;
     int incl = tb;
 #pragma unroll
@@ -167,7 +167,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Hq, int Hkv, int g,
-    int nr, float scale_log2, uint16_t* __restrict__ out, int32_t* __restrict__ dev_err) {
+    int nr, float scale_log2, uint16_t* __restrict__ out, int32_t* __restrict__ dev_err, int plan_early) {
   using LY = Layout<D>;
   // A staged partial row: O as D bf16 (unnormalised; one more rounding than the fp32
   // accumulator, far below the output's own bf16 rounding after the merge), then the running
@@ -222,10 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort;
 
-  // Everything above overlaps the previous kernel; R, Q and the cache are read from here on.
-  pdl_wait();
-  pdl_launch_dependents();
+  // Everything above overlaps the previous kernel; Q and the cache are read after the wait.
+  // Inside a step (plan_early) R was written by the select kernel, which finished before the
+  // scatter kernel released this one, so the plan is made before the wait (R is read through
+  // L2); standalone, R may come from the previous kernel.
+  if (!plan_early) pdl_wait();
   const Plan pl = make_plan(R, B, L, Hkv, nr, nclusters);
+  if (plan_early) pdl_wait();
+  pdl_launch_dependents();
   const bool split_mode = pl.splits > 1;
   Item split_item{};  // the shared tile's item, kept by the softmax warps for the merge
   split_item.nrows = -1;
@@ -583,8 +587,8 @@ bool encode_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, int rank, c
 
 template <int D>
 cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, const void* v_cache,
-                        const int32_t* R, float scale, void* out, void* ws, int32_t* dev_err, cudaStream_t s,
-                        ec_status* status) {
+                        const int32_t* R, float scale, void* out, void* ws, int32_t* dev_err, bool plan_early,
+                        cudaStream_t s, ec_status* status) {
   using LY = Layout<D>;
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) {
@@ -651,7 +655,7 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
   cfg.gridDim = dim3(mc * kCluster);
   cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, tq, tk, tv, R, p.B, p.L, p.Hq, p.Hkv, g, nr, scale * kLog2e,
-                         static_cast<uint16_t*>(out), dev_err);
+                         static_cast<uint16_t*>(out), dev_err, plan_early ? 1 : 0);
   if (e != cudaSuccess) *status = EC_ERR_CUDA;
   return e;
 }
@@ -665,10 +669,10 @@ size_t attention_workspace_bytes(const ec_params& p) {
 
 cudaError_t launch_partial_attention(const ec_params& p, const void* q, const void* k_cache,
                                      const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
-                                     int32_t* dev_err, cudaStream_t s, ec_status* status) {
+                                     int32_t* dev_err, bool plan_early, cudaStream_t s, ec_status* status) {
   *status = EC_OK;
-  if (p.D == 128) return launch_impl<128>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, s, status);
-  return launch_impl<64>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, s, status);
+  if (p.D == 128) return launch_impl<128>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, plan_early, s, status);
+  return launch_impl<64>(p, q, k_cache, v_cache, R, scale, out, ws, dev_err, plan_early, s, status);
 }
 
 }  // namespace ec

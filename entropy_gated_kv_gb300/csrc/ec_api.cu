@@ -183,7 +183,7 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
   if (ws_bytes < attention_workspace_bytes(*p)) return EC_ERR_INVALID_ARG;
   if (!(scale == scale)) return EC_ERR_INVALID_ARG;
   ec_status st = EC_OK;
-  launch_partial_attention(*p, q, k_cache, v_cache, R, scale, out, ws, dev_err, static_cast<cudaStream_t>(stream),
+  launch_partial_attention(*p, q, k_cache, v_cache, R, scale, out, ws, dev_err, false, static_cast<cudaStream_t>(stream),
                            &st);
   return st;
 }
@@ -237,7 +237,7 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
     if (e != cudaSuccess) return EC_ERR_CUDA;
     ec_status as = EC_OK;
     launch_partial_attention(*p, w + lay.qbuf, k_cache[l], v_cache[l], st->R, scale, out[l], w + lay.attn,
-                             st->dev_err, s, &as);
+                             st->dev_err, true, s, &as);
     if (as != EC_OK) return as;
   }
   return EC_OK;

@@ -58,9 +58,11 @@ cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, 
 
 // ---- partial attention --------------------------------------------------------------------
 size_t attention_workspace_bytes(const ec_params& p);
+// plan_early: R is final when the kernel starts (inside a step: written by the select kernel
+// two launches earlier), so the work plan is made before the grid dependency wait.
 cudaError_t launch_partial_attention(const ec_params& p, const void* q, const void* k_cache,
                                      const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
-                                     int32_t* dev_err, cudaStream_t s, ec_status* status);
+                                     int32_t* dev_err, bool plan_early, cudaStream_t s, ec_status* status);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

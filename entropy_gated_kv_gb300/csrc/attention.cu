@@ -52,6 +52,12 @@ constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxGrid = 256;
 constexpr int kCluster = 4;  // CTAs per cluster = KV splits of a shared tile
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+// Operand descriptors: every tile is 128-byte swizzled with 8-row groups 1024 bytes apart. One
+// K step of 16 keys / dims advances a K-major tile by 32 bytes within a 64-element atom (the
+// next atom is 16 KB further), and the MN-major V tile by 16 rows of 128 bytes.
+constexpr uint32_t kDescHi = sdesc_hi(1024);
+__host__ __device__ constexpr uint32_t step_qk(int kk) { return (kk >> 2) * (128 * 128 / 16) + (kk & 3) * 2; }
+constexpr uint32_t kStepPV = 16 * 128 / 16;
 
 struct Bars {
   uint64_t q_full, q_empty;
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
-    const uint32_t q_addr = smem_u32(q_smem);
+    const uint32_t q_lo = sdesc_lo(smem_u32(q_smem), 16);
     uint32_t it = 0;
     for (int n = 0;; ++n) {
       const int item = cta_item(n, pl, cluster, rank, nclusters);
@@ -286,13 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
                  mbar_wait_bounded(&bars->s_free[slot], (u & 1u) ^ 1u, abort_flag, dev_err, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t k_addr = smem_u32(smem + LY::kStageOff + slot * LY::kStageBytes);
+            const uint32_t k_lo = sdesc_lo(smem_u32(smem + LY::kStageOff + slot * LY::kStageBytes), 16);
+            const uint32_t s_col = tmem + kTmemS + slot * kBlockN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * LY::kAtomBytes + (kk & 3) * 32;
-              umma_bf16(tmem + kTmemS + slot * kBlockN, smem_desc_sw128(q_addr + off, 16, 1024),
-                        smem_desc_sw128(k_addr + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_ss(s_col, q_lo + step_qk(kk), k_lo + step_qk(kk), kDescHi, idesc_qk, kk > 0 ? 1u : 0u);
             umma_commit(&bars->s_full[slot]);
             if (j == I.nblk - 1) umma_commit(&bars->q_empty);
           }
@@ -303,12 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
             ok = ok && mbar_wait_bounded(&bars->p_full[ps], pu & 1u, abort_flag, dev_err, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t v_addr = smem_u32(smem + LY::kStageOff + ps * LY::kStageBytes + LY::kKVBytes);
+            const uint32_t v_lo =
+                sdesc_lo(smem_u32(smem + LY::kStageOff + ps * LY::kStageBytes + LY::kKVBytes), LY::kAtomBytes);
+            const uint32_t p_col = tmem + kTmemS + ps * kBlockN;
+            const uint32_t acc0 = j > 1 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk)  // P: 16 keys = 8 TMEM columns per product
-              umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + ps * kBlockN + kk * 8,
-                           smem_desc_sw128(v_addr + kk * 2048, LY::kAtomBytes, 1024), idesc_pv,
-                           (j > 1 || kk > 0) ? 1u : 0u);
+              umma_ts(tmem + kTmemO, p_col + kk * 8, v_lo + kk * kStepPV, kDescHi, idesc_pv, kk > 0 ? 1u : acc0);
             umma_commit(&bars->kv_empty[ps]);
             umma_commit(&bars->s_free[ps]);
             if (j == I.nblk) umma_commit(&bars->o_full);

@@ -46,6 +46,52 @@ NCOPY = 4
 CHUNK = 500
 
 
+# ---- multi-rank helpers (replicas: one independent step loop per rank, no data exchange) ----
+
+
+def init_ranks(world: int, backend: str | None = None) -> None:
+    """One process group for the timing barrier and reduction: NCCL when each rank has a GPU,
+    gloo otherwise, or the given backend (the CPU tests of this logic pass gloo)."""
+    if world <= 1:
+        return
+    import torch
+    import torch.distributed as dist
+
+    if backend is not None:
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    else:
+        dist.init_process_group("gloo")
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Barrier, then the largest of the ranks' timed-region lengths: the job's time at this N."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    dist.barrier()
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(world: int, steps: int, ms: float) -> float:
+    """Whole-job steps/s: each of the `world` ranks ran `steps` steps of its own replica in at
+    most `ms` milliseconds."""
+    return world * steps / (ms / 1e3)
+
+
 def kernel_source_hash(name: str) -> str:
     """Hash of a kernel's source file (ncu counters are only valid for the source they came from)."""
     import hashlib
@@ -260,9 +306,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     g_main.replay()  # one untimed replay to settle the graph
     torch.cuda.synchronize()
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    barrier(world)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
@@ -273,13 +317,7 @@ def run_ours(args, rank: int, world: int) -> dict | None:
             g_rem.replay()
         t1.record()
         torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     status, word = E.read_device_error(state_view(0).dev_err)
     if status != 0:
         raise RuntimeError(f"device error word {word:#x} during the timed steps")
@@ -432,7 +470,7 @@ def emit_ours(args, res, rank, world):
     pk = peaks()
     K = args.steps
     ms_per_step = res["ms"] / K
-    value = world * K / (res["ms"] / 1e3)
+    value = job_throughput(world, K, res["ms"])
     kern = res["kernels"]
     alg = algorithmic(w, kern["R"])
     ent_gbs = alg["entropy_decode_bytes"] / (kern["entropy_decode_us"] * 1e-6) / 1e9
@@ -618,12 +656,7 @@ def main():
         if rank == 0:
             run_reference(args)
         return
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
-        dist.init_process_group("nccl")
+    init_ranks(world)
     res = run_ours(args, rank, world)
     if rank == 0:
         emit_ours(args, res, rank, world)

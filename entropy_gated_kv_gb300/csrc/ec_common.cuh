@@ -288,6 +288,23 @@ EC_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_depend
 
 namespace ec {
 
+// Bulk copy from global memory to this CTA's shared memory (the async copy engine, no tensor
+// map); completion is counted in bytes on `bar`. Both addresses 16-byte aligned, size a
+// multiple of 16. evict_first: the source is read once, so it should leave L2 first.
+EC_DEV void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t l2_policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(l2_policy)
+      : "memory");
+}
+
+EC_DEV uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Bulk copy from this CTA's shared memory to (possibly another CTA's) shared memory in the
 // cluster; completion is counted in bytes on the destination's mbarrier. Addresses 16-byte
 // aligned, size a multiple of 16.

@@ -74,6 +74,6 @@ extern "C" ec_status ec_entropy_decode_noalloc(const void* logits, int64_t row_s
       return EC_ERR_CUDA;
   }
   const cudaError_t e = ec::launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf,
-                                                  scratch, nullptr, 1, true, false, s);
+                                                  scratch, nullptr, 1, true, false, nullptr, s);
   return e == cudaSuccess ? EC_OK : EC_ERR_CUDA;
 }

@@ -137,3 +137,13 @@ def test_partial_step_with_short_history_and_ragged_candidates(E):
     flags = run_and_check(E, w, st_h, lg, W.layer_tensors(w, 0))
     assert int(st_h["ring_count"][0]) < w.k
     assert len(flags) == 1
+
+
+def test_large_vocabulary_step_with_short_candidate_lists(E):
+    # Dream-7B-shaped batch (78 MB of logits: the decode stage streams through persistent
+    # CTAs) where sequences list fewer candidates than C_max, one none at all: the skipped
+    # rows must be left out of the decode, the commit and the gate.
+    w = W.workload(3)
+    st_h = W.snapshot_state(w)
+    st_h["cand_count"][:] = np.array([32, 5, 0, 17, 32, 1, 31, 32], dtype=st_h["cand_count"].dtype)
+    run_and_check(E, w, st_h, W.step_logits(w), W.layer_tensors(w, 0), sample_rows=32)

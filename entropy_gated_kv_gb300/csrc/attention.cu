@@ -487,8 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
                             dsmem_map(smem_u32(&bars->recv), dst));
       }
     }
+    // The barrier that keeps every CTA alive until the pushes out of its `send` have landed is
+    // split: a CTA's merging threads arrive once their own receive barrier is complete (every
+    // push into them has finished reading its source), the others right away, and everyone
+    // waits at teardown, so the barrier's latency overlaps the merge.
+    if (warp < 2) cluster_arrive_release();
     if (warp >= 2) {
       const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->recv, 0, abort_flag, dev_err, kWaitLimitNs));
+      cluster_arrive_release();
       if (got && cluster < pl.tiles) {
         // the tile is shared by the cluster; CTAs without a split of their own decode it here
         const Item I = split_item.nrows >= 0 ? split_item : decode_item(cluster * pl.splits, pl, R, B, L, Hkv, nr);
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
         }
       }
     }
-    cluster_sync_all();  // every push has landed and been read before any CTA leaves
+    cluster_wait_acquire();  // every push out of this CTA has landed before it leaves
   }
 
   // ---------------------------------------------------------------------- teardown

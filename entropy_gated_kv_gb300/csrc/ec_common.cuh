@@ -252,6 +252,11 @@ EC_DEV uint32_t cluster_size() {
 EC_DEV void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+
+// The two halves of a cluster barrier, for work between them (every thread of every CTA
+// arrives once, then waits once; warps may be at different points, hence not .aligned).
+EC_DEV void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+EC_DEV void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 // Address of the same shared-memory location in the CTA of the given rank.
 EC_DEV uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
   uint32_t r;

@@ -89,6 +89,7 @@ struct Plan {
   int splits;  // key splits per tile
   int bps;     // KV blocks per split
   int nkv;     // KV blocks per sequence
+  int r_lane;  // B <= 32: clamped R[lane] (0 past B), so items decode without reading R again
 };
 
 struct Item {
@@ -107,10 +108,15 @@ __device__ __forceinline__ int warp_sum(int v) {
 // clusters, each cluster shares one tile over kCluster key splits; otherwise no split.
 __device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int nclusters) {
   const int lane = threadIdx.x & 31;
-  int t = 0;
-  for (int b = lane; b < B; b += 32) t += Hkv * ((clamp_r(__ldcg(R + b), L) + nr - 1) / nr);
+  int t = 0, r_lane = 0;
+  for (int b = lane; b < B; b += 32) {
+    const int rb = clamp_r(__ldcg(R + b), L);
+    if (b == lane) r_lane = rb;
+    t += Hkv * ((rb + nr - 1) / nr);
+  }
   t = warp_sum(t);
   Plan p;
+  p.r_lane = r_lane;
   p.tiles = t;
   p.nkv = (L + kBlockN - 1) / kBlockN;
   const int s = (t > 0 && t <= nclusters) ? min(kCluster, p.nkv) : 1;
@@ -137,7 +143,7 @@ __device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, i
   int base = 0;
   for (int b0 = 0; b0 < B; b0 += 32) {
     const int b = b0 + lane;
-    const int rb = b < B ? clamp_r(__ldcg(R + b), L) : 0;
+    const int rb = b >= B ? 0 : (B <= 32 ? pl.r_lane : clamp_r(__ldcg(R + b), L));
     const int tb = b < B ? Hkv * ((rb + nr - 1) / nr) : 0;
     int incl = tb;
 #pragma unroll

@@ -111,15 +111,16 @@ def profiled_traffic(kernel: str, source: str) -> float | None:
         return None
 
 
-def run_profile(steps: int) -> None:
-    """A few eager steps of the workload (no graphs, no timing): a short program for ncu."""
+def run_profile(steps: int, workload: int = WORKLOAD) -> None:
+    """A few eager steps of the workload (no graphs, no timing), then as many calls of the
+    standalone decode entry on the step's logits: a short program for ncu."""
     import torch
 
     import entropy_gated_kv_gb300 as E
     from entropy_gated_kv_gb300 import build as B
 
     B.build()
-    w = W.workload(WORKLOAD)
+    w = W.workload(workload)
     p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
                  logits_dtype=w.logits_dtype)
     st_h = W.snapshot_state(w)
@@ -130,7 +131,8 @@ def run_profile(steps: int) -> None:
 
     layer = {n: bf(lay[n]) for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
     layer["out"] = torch.zeros(w.B, w.L, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
-    logits = bf(W.step_logits(w))
+    lg_h = W.step_logits(w)
+    logits = bf(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(np.ascontiguousarray(lg_h)).cuda()
     cp = torch.from_numpy(st_h["cand_pos"]).cuda()
     cc = torch.from_numpy(st_h["cand_count"]).cuda()
     ws = E.workspace(E.step_workspace_size(p))
@@ -138,6 +140,10 @@ def run_profile(steps: int) -> None:
         st = E.DecodeState.from_arrays(p, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
                                        ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
         E.step(p, st, logits, cp, cc, [layer], ws=ws)
+    rows = logits.view(-1, w.V)
+    ews = E.workspace(E.entropy_decode_workspace_size(rows.shape[0], w.V, rows.dtype))
+    for _ in range(steps):
+        E.entropy_decode(rows, ws=ews)
     torch.cuda.synchronize()
     status, word = E.read_device_error(st.dev_err)
     print(json.dumps({"profile_steps": steps, "R": int(st.R[0]), "flag": int(st.flag[0]), "status": status}))
@@ -646,7 +652,7 @@ def main():
                     help="run this many eager steps and exit (a short program for ncu)")
     args = ap.parse_args()
     if args.profile_steps > 0:
-        run_profile(args.profile_steps)
+        run_profile(args.profile_steps, args.workload)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -29,9 +29,9 @@ size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype);
 // the one-CTA-per-chunk launch runs, whose small independent CTAs become resident while a
 // large predecessor kernel is still running (the better choice inside a chain of kernels).
 // publish_only: the chunk partials (max, index, S, T) are written to the workspace and the
-// next kernel merges them (ids / entropy / log_conf are not written). Problems of 32 MB and
-// more stream through persistent CTAs instead (same workspace layout). dev_err (may be null):
-// where a timed-out wait of the streaming path is reported.
+// next kernel merges them (ids / entropy / log_conf are not written). Outside publish-only
+// mode, problems of 32 MB and more stream through persistent CTAs (same workspace layout).
+// dev_err (may be null): where a timed-out wait of the streaming path is reported.
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
                                   const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,

@@ -26,7 +26,7 @@
 //     each chunk publishes its partial to the workspace and the last chunk of a row to finish
 //     (a counter per row, no spinning) merges them, writes the row result and returns the
 //     counter to zero.
-//   - Problems of 32 MB and more: one persistent CTA of 16 warps per SM; each warp streams a
+//   - Problems of 32 MB and more, outside a step: one persistent CTA of 16 warps per SM; each warp streams a
 //     contiguous run of the same chunks through a ring of three 4 KB shared-memory stages
 //     filled by bulk async copies (cp.async.bulk, completion on an mbarrier), keeps a running
 //     (max, index, S, T) per lane and merges once per row segment; the segments publish in
@@ -863,7 +863,9 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int64_t total_bytes = static_cast<int64_t>(n_rows) * V * (f32 ? 4 : 2);
-  if (ws != nullptr && nch > 1 && total_bytes >= kStreamMinBytes) {
+  // not in publish-only mode (inside a step): the persistent CTAs cannot start beside the
+  // previous kernel, and the split CTAs can
+  if (!publish_only && ws != nullptr && nch > 1 && total_bytes >= kStreamMinBytes) {
     const int64_t units = static_cast<int64_t>(n_rows) * nch;
     const int grid = static_cast<int>(std::min<int64_t>(sms, (units + kStreamWarps - 1) / kStreamWarps));
     if (f32) return launch_stream<EC_F32>(grid, s, a);

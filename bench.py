@@ -113,7 +113,8 @@ def profiled_traffic(kernel: str, source: str) -> float | None:
 
 def run_profile(steps: int, workload: int = WORKLOAD) -> None:
     """A few eager steps of the workload (no graphs, no timing), then as many calls of the
-    standalone decode entry on the step's logits: a short program for ncu."""
+    standalone decode entry on the step's logits and of the output projection fused with the
+    decode: a short program for ncu."""
     import torch
 
     import entropy_gated_kv_gb300 as E
@@ -144,6 +145,12 @@ def run_profile(steps: int, workload: int = WORKLOAD) -> None:
     ews = E.workspace(E.entropy_decode_workspace_size(rows.shape[0], w.V, rows.dtype))
     for _ in range(steps):
         E.entropy_decode(rows, ws=ews)
+    if w.d_model > 0:  # and the output projection fused with the decode, on a random weight
+        g = torch.Generator(device="cuda").manual_seed(w.seed)
+        hid = torch.randn(rows.shape[0], w.d_model, device="cuda", generator=g).to(torch.bfloat16)
+        wt = (torch.randn(w.V, w.d_model, device="cuda", generator=g) / w.d_model ** 0.5).to(torch.bfloat16)
+        for _ in range(steps):
+            E.lm_head_entropy(hid, wt)
     torch.cuda.synchronize()
     status, word = E.read_device_error(st.dev_err)
     print(json.dumps({"profile_steps": steps, "R": int(st.R[0]), "flag": int(st.flag[0]), "status": status}))
@@ -397,6 +404,20 @@ def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
         torch.cuda.synchronize()
         return a.elapsed_time(b) * 1e3 / (reps * G)  # us per launch
 
+    # stage (a) from the hidden states: the output projection fused with the decode, on a
+    # random bf16 weight of the model's shape (V x d_model, about 1 GB: no L2 reuse)
+    if w.d_model > 0:
+        g = torch.Generator(device=dev).manual_seed(w.seed)
+        hid = torch.randn(rows, w.d_model, device=dev, generator=g).to(torch.bfloat16)
+        wt = (torch.randn(w.V, w.d_model, device=dev, generator=g) / w.d_model ** 0.5).to(torch.bfloat16)
+        lm_ws = E.workspace(E.lm_head_entropy_workspace_size(rows), dev)
+
+        def stage_lm_head(i):
+            E.lm_head_entropy(hid, wt, ws=lm_ws, out=(ids, ent, conf))
+
+        out["lm_head_entropy_us"] = timed(stage_lm_head, min(n, 200))
+        out["lm_head_bytes"] = (w.V + rows) * w.d_model * 2
+        del wt
     out["entropy_decode_us"] = timed(stage_entropy, n)
     out["partial_attention_us"] = timed(stage_attention, n)
     out["kv_scatter_us"] = timed(stage_scatter, n)
@@ -526,6 +547,10 @@ def emit_ours(args, res, rank, world):
         "gpu_launches": 4 * K,
         "clocks": res["clocks"],
     }
+    if "lm_head_entropy_us" in kern:  # not part of the timed step, which starts from logits
+        lm_gbs = kern["lm_head_bytes"] / (kern["lm_head_entropy_us"] * 1e3)
+        line["kernels"]["lm_head_entropy"] = {"us": kern["lm_head_entropy_us"], "GB/s": lm_gbs,
+                                              "frac_hbm": lm_gbs / pk["hbm_gbs"], "d_model": w.d_model}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
     print(json.dumps(line))

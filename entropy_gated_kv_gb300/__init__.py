@@ -171,6 +171,35 @@ def entropy_decode_noalloc(logits: torch.Tensor, V: int | None = None, out: tupl
     return out
 
 
+def lm_head_entropy_workspace_size(n_rows: int) -> int:
+    return int(lib().ec_lm_head_entropy_workspace_size(n_rows))
+
+
+def lm_head_entropy(hidden: torch.Tensor, weight: torch.Tensor, ws: torch.Tensor | None = None,
+                    out: tuple | None = None, stream=None):
+    """(a) from the hidden states: ids, entropy, log_conf of logits = hidden @ weight.T, which
+    are computed on the tensor cores and never stored. hidden [n_rows, d_model] and weight
+    [V, d_model]: contiguous CUDA bf16."""
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise ValueError("hidden and weight must be bf16")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden [n_rows, d_model] and weight [V, d_model]")
+    if not (hidden.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("hidden and weight must be contiguous")
+    n, d = hidden.shape
+    V = weight.shape[0]
+    if out is None:
+        out = (torch.empty(n, dtype=torch.int32, device=hidden.device),
+               torch.empty(n, dtype=torch.float32, device=hidden.device),
+               torch.empty(n, dtype=torch.float32, device=hidden.device))
+    if ws is None:
+        ws = workspace(lm_head_entropy_workspace_size(n), hidden.device)
+    st = lib().ec_lm_head_entropy(_vp(hidden), _vp(weight), n, d, V, _vp(out[0]), _vp(out[1]), _vp(out[2]), _vp(ws),
+                                  ws.numel(), _stream(stream))
+    C.check(st, "ec_lm_head_entropy")
+    return out
+
+
 def select_recompute(p: Params, state: DecodeState, cand_pos, cand_count, ids, entropy, log_conf, stream=None):
     """(b)+(c) commit, gate, history push and recompute set; updates `state` in place."""
     pc, sc = p.c(), state.c()

@@ -139,6 +139,24 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
                                            nullptr, 1, true, false, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- (a) from the hidden states ----------------------------------------------------------------
+size_t ec_lm_head_entropy_workspace_size(int32_t n_rows) {
+  if (n_rows < 1 || n_rows > lm_head_max_rows()) return 0;
+  return lm_head_workspace_bytes(n_rows);
+}
+
+ec_status ec_lm_head_entropy(const void* hidden, const void* weight, int32_t n_rows, int32_t d_model, int32_t V,
+                             int32_t* ids, float* entropy, float* log_conf, void* ws, size_t ws_bytes,
+                             ec_stream_t stream) {
+  if (n_rows < 1 || n_rows > lm_head_max_rows()) return EC_ERR_INVALID_ARG;
+  if (d_model < 64 || d_model > 65536 || d_model % 64 != 0 || V < 1 || V > kMaxV) return EC_ERR_INVALID_ARG;
+  if (!hidden || !weight || !ids || !entropy || !log_conf || !ws) return EC_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(ws)) return EC_ERR_INVALID_ARG;
+  if (ws_bytes < lm_head_workspace_bytes(n_rows)) return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_lm_head_entropy(hidden, weight, n_rows, d_model, V, ids, entropy, log_conf, ws, nullptr,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 // ---- (b)+(c) --------------------------------------------------------------------------------
 ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int32_t* cand_pos,
                               const int32_t* cand_count, const int32_t* ids, const float* entropy,

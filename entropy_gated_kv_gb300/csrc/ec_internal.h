@@ -37,6 +37,13 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
                                   const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
                                   bool publish_only, int32_t* dev_err, cudaStream_t s);
 
+// ---- output projection fused with the decode (lm_head_entropy.cu) -------------------------
+size_t lm_head_workspace_bytes(int32_t n_rows);
+int32_t lm_head_max_rows();
+cudaError_t launch_lm_head_entropy(const void* hidden, const void* weight, int32_t n_rows, int32_t d_model, int32_t V,
+                                   int32_t* ids, float* entropy, float* log_conf, void* ws, int32_t* dev_err,
+                                   cudaStream_t s);
+
 // ---- select_recompute ---------------------------------------------------------------------
 struct SelArgs;
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,

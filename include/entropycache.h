@@ -175,6 +175,26 @@ ec_status ec_entropy_decode_noalloc(const void* logits, int64_t row_stride, int3
                                     int32_t dtype, int32_t* ids, float* entropy, float* log_conf,
                                     ec_stream_t stream);
 
+/* ---- (a) from the hidden states: output projection fused with the decode ---------------
+ * Stage (a) of the step (EntropyCache, gist.science zh summary §2.2: decode each masked
+ * candidate and take the entropy of its softmax) applied to logits that are computed here
+ * and never stored: logits[r, v] = sum_k hidden[r, k] * weight[v, k], accumulated in fp32
+ * from bf16 products on the tensor cores. The pages leave this product to the model (its
+ * output projection); fusing it with the decode has no counterpart in the pages.
+ *   hidden  [n_rows, d_model] bf16, row-major, contiguous, 16-byte aligned (device).
+ *   weight  [V, d_model] bf16, row-major, contiguous, 16-byte aligned (device).
+ *   ids, entropy, log_conf [n_rows]: as ec_entropy_decode (greedy id, lowest index on ties;
+ *            entropy in nats; ln of the decoded token's probability).
+ *   ws       device workspace of ec_lm_head_entropy_workspace_size(n_rows) bytes, 16-byte
+ *            aligned; no initial contents needed. Calls sharing a workspace must not overlap.
+ * 1 <= n_rows <= 256; d_model a multiple of 64 (64 .. 65536); 1 <= V <= 2^30.
+ * EC_ERR_INVALID_ARG for a bad argument (nothing launched). A wait inside the kernel that
+ * gives up (never expected) makes the affected rows' entropy NaN. */
+size_t ec_lm_head_entropy_workspace_size(int32_t n_rows);
+ec_status ec_lm_head_entropy(const void* hidden, const void* weight, int32_t n_rows, int32_t d_model, int32_t V,
+                             int32_t* ids, float* entropy, float* log_conf, void* ws, size_t ws_bytes,
+                             ec_stream_t stream);
+
 /* ---- (b)+(c) commit, max-entropy gate, decode history, recompute set -------------------
  * Follows the skip decision and selection stage of the workflow (zh summary §2.2: full
  * recompute iff E_{t+1} = max over newly decoded tokens of their entropy exceeds tau,

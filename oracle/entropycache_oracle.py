@@ -39,6 +39,7 @@ __all__ = [
     "widen",
     "entropy_decode_row",
     "entropy_decode",
+    "lm_head_entropy",
     "select_decoded",
     "max_entropy",
     "recompute_flag",
@@ -97,6 +98,18 @@ def entropy_decode(logits: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarr
     for i in range(n):
         ids[i], ent[i], conf[i] = entropy_decode_row(logits[i])
     return ids, ent, conf
+
+
+def lm_head_entropy(hidden: np.ndarray, weight: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Stage (a) on logits produced from the candidates' hidden states.
+
+    logits = hidden @ weight.T (hidden [n_rows, d_model], weight [V, d_model], float64), then
+    entropy_decode of those logits ([zh] §2.2). The pages leave the product to the model (its
+    output projection); the library computes it fused with the decode, and this is the plain
+    composition it must match.
+    """
+    logits = np.asarray(hidden, dtype=np.float64) @ np.asarray(weight, dtype=np.float64).T
+    return entropy_decode(logits)
 
 
 # --------------------------------------------------------------------------------------

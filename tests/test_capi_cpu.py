@@ -165,3 +165,28 @@ def test_binding_refuses_cpu_tensors(capi):
 
     with pytest.raises(ValueError):
         E.entropy_decode(torch.zeros(2, 64))
+
+
+def test_lm_head_entropy_validation(capi):
+    lib = capi.load()
+    INV = capi.EC_ERR_INVALID_ARG
+    assert lib.ec_lm_head_entropy_workspace_size(0) == 0
+    assert lib.ec_lm_head_entropy_workspace_size(257) == 0
+    assert lib.ec_lm_head_entropy_workspace_size(32) >= 32 * 16
+    p = 1 << 20  # never dereferenced: every call below fails validation first
+    ws = lib.ec_lm_head_entropy_workspace_size(32)
+    ok = dict(hidden=p, weight=p, n_rows=32, d_model=4096, V=126464, ids=p, ent=p, conf=p, ws=p, ws_bytes=ws)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.ec_lm_head_entropy(a["hidden"], a["weight"], a["n_rows"], a["d_model"], a["V"], a["ids"],
+                                      a["ent"], a["conf"], a["ws"], a["ws_bytes"], None)
+
+    assert call(n_rows=0) == INV
+    assert call(n_rows=257) == INV
+    assert call(d_model=100) == INV  # not a multiple of 64
+    assert call(d_model=0) == INV
+    assert call(V=0) == INV
+    assert call(hidden=None) == INV
+    assert call(weight=p + 8) == INV  # not 16-byte aligned
+    assert call(ws_bytes=ws - 1) == INV

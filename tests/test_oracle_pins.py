@@ -343,3 +343,35 @@ def test_step_full_flag_attention_is_dense_attention():
     out = got["layers"][0]["out"]
     dense = _sdpa(lay["q_src"], lay["k_src"], lay["v_src"], 1.0 / math.sqrt(D))
     np.testing.assert_allclose(out, dense, rtol=1e-12, atol=1e-12)
+
+
+# ---- (a) from hidden states: logits = hidden @ weight.T, then the decode -----------------
+
+
+def test_lm_head_entropy_closed_forms_and_orientation():
+    # hidden = identity rows, so logits row r is column r of weight: the rows below are logs
+    # of small integers with closed-form entropies (softmax = the integers over their sum).
+    # weight is not symmetric, so a transposed product would give other entropies.
+    rows = [[1, 1, 1, 1], [1, 1, 2, 4], [12, 2, 1, 1], [1, 1, 1, 5]]
+    logits = np.log(np.array(rows, dtype=np.float64))
+    weight = logits.T.copy()  # [V = 4, d_model = 4]
+    hidden = np.eye(4)
+    ids, ent, conf = O.lm_head_entropy(hidden, weight)
+    ln2, ln3, ln5 = math.log(2), math.log(3), math.log(5)
+    np.testing.assert_array_equal(ids, [0, 3, 0, 3])
+    np.testing.assert_allclose(ent, [2 * ln2, 1.75 * ln2, 19 / 8 * ln2 - 0.75 * ln3, 3 * ln2 - 5 / 8 * ln5],
+                               rtol=1e-13)
+    np.testing.assert_allclose(conf, [-2 * ln2, -ln2, ln3 - 2 * ln2, ln5 - 3 * ln2], rtol=1e-13)
+
+
+def test_lm_head_entropy_brute_force_dot_products():
+    rng = np.random.default_rng(7)
+    for n, d, V in [(1, 1, 1), (3, 5, 7), (4, 16, 33)]:
+        h = rng.standard_normal((n, d))
+        w = rng.standard_normal((V, d))
+        logits = [[sum(h[r, k] * w[v, k] for k in range(d)) for v in range(V)] for r in range(n)]
+        want = O.entropy_decode(np.array(logits))
+        got = O.lm_head_entropy(h, w)
+        np.testing.assert_array_equal(got[0], want[0])
+        np.testing.assert_allclose(got[1], want[1], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(got[2], want[2], rtol=1e-12, atol=1e-14)

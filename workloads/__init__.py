@@ -71,6 +71,7 @@ class Workload:
     n_layers: int = 1
     steps: int = 1
     seed: int = 0
+    d_model: int = 0  # hidden size of the model's output projection (Hq * D for these models)
 
     @property
     def C_max(self) -> int:
@@ -83,19 +84,19 @@ class Workload:
 WORKLOADS: dict[int, Workload] = {
     1: Workload(1, "tiny", B=1, L=256, prompt=128, gen=128, block=32, Hq=8, Hkv=8, D=64,
                 V=32000, k=16, n_dec=1, tau=1.0, logits_dtype="f32",
-                logits_kind="gauss_scale", seed=1),
+                logits_kind="gauss_scale", seed=1, d_model=512),
     2: Workload(2, "llada_layer", B=1, L=1024, prompt=768, gen=256, block=32, Hq=32, Hkv=32,
                 D=128, V=126464, k=64, n_dec=1, tau=1.0, logits_dtype="bf16",
-                logits_kind="gauss_scale", seed=2),
+                logits_kind="gauss_scale", seed=2, d_model=4096),
     3: Workload(3, "dream_gqa", B=8, L=2048, prompt=1792, gen=256, block=32, Hq=28, Hkv=4,
                 D=128, V=152064, k=64, n_dec=1, tau=1.0, logits_dtype="bf16",
-                logits_kind="zipf", seed=3),
+                logits_kind="zipf", seed=3, d_model=3584),
     4: Workload(4, "llada_trace", B=4, L=4096, prompt=3840, gen=256, block=32, Hq=32,
                 Hkv=32, D=128, V=126464, k=64, n_dec=1, tau=1.0, logits_dtype="bf16",
-                logits_kind="trace", n_layers=32, steps=256, seed=4),
+                logits_kind="trace", n_layers=32, steps=256, seed=4, d_model=4096),
     5: Workload(5, "long_context", B=1, L=32768, prompt=32512, gen=256, block=32, Hq=32,
                 Hkv=32, D=128, V=126464, k=64, n_dec=1, tau=1.0, logits_dtype="bf16",
-                logits_kind="gauss_scale", seed=5),
+                logits_kind="gauss_scale", seed=5, d_model=4096),
 }
 
 
@@ -269,3 +270,25 @@ def layer_tensors(w: Workload, layer: int = 0, pool: dict | None = None) -> dict
         flat = a.reshape(-1)
         out[name] = np.roll(flat, shift % flat.size).reshape(a.shape)
     return out
+
+
+def lm_head_inputs(n_rows: int, d_model: int, V: int, seed: int = 0, peaked: int = 0,
+                   chunk_rows: int = 8192) -> tuple[np.ndarray, np.ndarray]:
+    """Hidden states and an output-projection matrix, as bf16 bit patterns.
+
+    weight [V, d_model] ~ N(0, 1 / d_model) (the usual initialisation scale, so logits are about
+    N(0, 1)); hidden [n_rows, d_model] ~ N(0, 1). The first `peaked` rows get a large component
+    along a seeded weight row, a confident prediction. Generated in float32 chunks of
+    `chunk_rows` vocabulary rows so that a full-size matrix never exists in float64.
+    """
+    r = rng_for(seed, 41)
+    weight = np.empty((V, d_model), dtype=np.uint16)
+    for v0 in range(0, V, chunk_rows):
+        v1 = min(V, v0 + chunk_rows)
+        weight[v0:v1] = to_bf16_bits(r.standard_normal((v1 - v0, d_model), dtype=np.float32) / np.sqrt(d_model))
+    hidden = r.standard_normal((n_rows, d_model))
+    for i in range(min(peaked, n_rows)):
+        v = int(r.integers(0, V))
+        wv = bf16_bits_to_f32(weight[v]).astype(np.float64)
+        hidden[i] += (12.0 + i) * wv / max(float(wv @ wv), 1e-30)
+    return to_bf16_bits(hidden), weight

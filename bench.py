@@ -425,58 +425,125 @@ def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
     return out
 
 
-def run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n) -> dict:
-    """ec_step end to end from pinned host buffers: every step copies its inputs host->device
-    and reads its results back (eager launches, one stream)."""
+def flat_state(E, p, dev, **arrays):
+    """A DecodeState whose fields are views of one flat device buffer (256-byte aligned), so
+    that it is restored with one copy; E, flag and R are adjacent at the end, so that they read
+    back as one slice. Returns (state, flat buffer, (start, end) byte range of E..R)."""
     import torch
 
-    def pinned(a, dt=None):
-        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if dt is None else np.ascontiguousarray(a))
-        return t.pin_memory()
+    B, L, k = p.B, p.L, p.k
+    spec = [("tokens", torch.int32, (B, L)), ("mask", torch.uint8, (B, L)), ("ring", torch.int32, (B, k)),
+            ("ring_head", torch.int32, (B,)), ("ring_count", torch.int32, (B,)), ("dec_pos", torch.int32, (B, p.n_dec)),
+            ("idx", torch.int32, (B, L)), ("dev_err", torch.int32, (1,)), ("E", torch.float32, (B,)),
+            ("flag", torch.int32, (B,)), ("R", torch.int32, (B,))]
+    offs, off = {}, 0
+    for name, dt, shape in spec:
+        nb = int(np.prod(shape)) * torch.tensor([], dtype=dt).element_size()
+        offs[name] = (off, nb)
+        off += (nb + 255) // 256 * 256 if name not in ("E", "flag") else nb
+    flat = torch.zeros(off, dtype=torch.uint8, device=dev)
+    st = object.__new__(E.DecodeState)
+    for name, dt, shape in spec:
+        o, nb = offs[name]
+        t = flat[o:o + nb].view(dt).view(shape)
+        setattr(st, name, t)
+    # flag is one byte per sequence in the ABI: keep a uint8 view over the first bytes of its slot
+    o, _ = offs["flag"]
+    st.flag = flat[o:o + B]
+    for name, a in arrays.items():
+        getattr(st, name).copy_(torch.as_tensor(a).to(getattr(st, name).dtype))
+    return st, flat, (offs["E"][0], offs["R"][0] + offs["R"][1])
 
-    h = {n: pinned(lay_h[n]) for n in ("k_src", "v_src", "q_src")}
-    h["logits"] = pinned(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(lg_h).pin_memory()
-    d = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in h.items()}
+
+def run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n) -> dict:
+    """ec_step end to end from pinned host buffers, pipelined as a serving loop would run it:
+    every step copies its inputs host->device (one copy of one pinned blob) and reads its
+    results back (the output rows and R / flag / E), with step i+1's upload and step i-1's
+    readback on two copy streams overlapping step i's kernels. Device inputs and outputs are
+    double-buffered; events order each buffer's reuse."""
+    import torch
+
+    bf = torch.bfloat16
+    parts = [("logits", lg_h)] + [
+        (k_, lay_h[k_]) for k_ in ("k_src", "v_src", "q_src")]
+    offs, off = {}, 0
+    for k_, a in parts:
+        nb = np.ascontiguousarray(a).nbytes
+        offs[k_] = (off, nb, a.shape)
+        off += (nb + 255) // 256 * 256
+    blob_h = torch.empty(off, dtype=torch.uint8).pin_memory()
+    for k_, a in parts:
+        o, nb, _ = offs[k_]
+        blob_h[o:o + nb].copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)))
+    blob_d = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def view(blob, k_, dt):
+        o, nb, shape = offs[k_]
+        return blob[o:o + nb].view(dt).view(shape)
+
     kc = torch.from_numpy(lay_h["k_cache"].view(np.int16)).to(dev)
     vc = torch.from_numpy(lay_h["v_cache"].view(np.int16)).to(dev)
-    out = torch.empty(w.B, w.L, w.Hq, w.D, dtype=torch.int16, device=dev)
-    out_h = torch.empty(out.shape, dtype=torch.int16).pin_memory()
-    small_h = torch.empty(3 * w.B, dtype=torch.int32).pin_memory()
+    out = [torch.empty(w.B, w.L, w.Hq, w.D, dtype=bf, device=dev) for _ in range(2)]
+    out_h = [torch.empty(w.B, w.L, w.Hq, w.D, dtype=bf).pin_memory() for _ in range(2)]
     cand_pos = torch.from_numpy(st_h["cand_pos"]).to(dev)
     cand_count = torch.from_numpy(st_h["cand_count"]).to(dev)
     ws = E.workspace(E.step_workspace_size(p), dev)
-    pristine = E.DecodeState.from_arrays(p, device=dev, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
-                                         ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
-    st = pristine.clone()
-    bf = torch.bfloat16
-    h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = out.numel() * 2 + small_h.numel() * 4
+    init = dict(tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"], ring_head=st_h["ring_head"],
+                ring_count=st_h["ring_count"])
+    _, pristine_flat, _ = flat_state(E, p, dev, **init)
+    st, st_flat, (r0, r1) = flat_state(E, p, dev, **init)
+    small = [torch.empty(r1 - r0, dtype=torch.uint8, device=dev) for _ in range(2)]
+    small_h = [torch.empty(r1 - r0, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    h2d = off
+    d2h = out[0].numel() * 2 + (r1 - r0)
+    s_in, s_cp, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
 
-    def step():
-        for f in E.DecodeState.FIELDS:
-            getattr(st, f).copy_(getattr(pristine, f), non_blocking=True)
-        for k_, t in h.items():
-            d[k_].copy_(t, non_blocking=True)
-        E.step(p, st, d["logits"].view(bf) if w.logits_dtype == "bf16" else d["logits"], cand_pos, cand_count,
-               [dict(k_cache=kc.view(bf), v_cache=vc.view(bf), k_src=d["k_src"].view(bf), v_src=d["v_src"].view(bf),
-                     q_src=d["q_src"].view(bf), out=out.view(bf))], ws=ws)
-        out_h.copy_(out, non_blocking=True)
-        small_h[: w.B].copy_(st.R, non_blocking=True)
-        small_h[w.B: 2 * w.B].copy_(st.flag.to(torch.int32), non_blocking=True)
-        small_h[2 * w.B:].copy_(st.E.view(torch.int32), non_blocking=True)
+    def step(i):
+        sl = i & 1
+        with torch.cuda.stream(s_in):
+            if started[sl]:
+                s_in.wait_event(done[sl])  # the step two back has consumed this input buffer
+            blob_d[sl].copy_(blob_h, non_blocking=True)
+            in_ready[sl].record(s_in)
+        with torch.cuda.stream(s_cp):
+            s_cp.wait_event(in_ready[sl])
+            if started[sl]:
+                s_cp.wait_event(out_read[sl])  # its outputs have been read back
+            st_flat.copy_(pristine_flat, non_blocking=True)  # the same starting state every step
+            lg = view(blob_d[sl], "logits", bf if w.logits_dtype == "bf16" else torch.float32)
+            E.step(p, st, lg, cand_pos, cand_count,
+                   [dict(k_cache=kc.view(bf), v_cache=vc.view(bf), k_src=view(blob_d[sl], "k_src", bf),
+                         v_src=view(blob_d[sl], "v_src", bf), q_src=view(blob_d[sl], "q_src", bf), out=out[sl])],
+                   ws=ws, stream=s_cp)
+            small[sl].copy_(st_flat[r0:r1], non_blocking=True)  # E, flag, R
+            done[sl].record(s_cp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[sl])
+            out_h[sl].copy_(out[sl], non_blocking=True)
+            small_h[sl].copy_(small[sl], non_blocking=True)
+            out_read[sl].record(s_out)
+        started[sl] = True
 
-    for _ in range(3):
-        step()
+    for i in range(4):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        step()
-    b.record()
+    cur = torch.cuda.current_stream(dev)
+    a.record(cur)
+    for s_ in (s_in, s_cp, s_out):
+        s_.wait_stream(cur)
+    for i in range(n):
+        step(i)
+    for s_ in (s_in, s_cp, s_out):
+        cur.wait_stream(s_)
+    b.record(cur)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
     return {"value": n / (ms / 1e3), "unit": "steps/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": n}
+            "steps": n, "pipelined": "upload of step i+1 and readback of step i-1 overlap step i"}
 
 
 def algorithmic(w, R) -> dict:

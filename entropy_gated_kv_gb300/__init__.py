@@ -264,6 +264,13 @@ def step(p: Params, state: DecodeState, logits, cand_pos, cand_count, layers: li
     C.check(st, "ec_step")
 
 
+def selftest_bounded_wait(dev_err: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """Runs the library's bounded wait on a barrier nothing completes; afterwards dev_err
+    holds EC_DEVERR_TIMEOUT (read it with read_device_error)."""
+    st = lib().ec_selftest_bounded_wait(_vp(dev_err), int(limit_ns), _stream(stream))
+    C.check(st, "ec_selftest_bounded_wait")
+
+
 def read_device_error(dev_err: torch.Tensor, stream=None) -> tuple[int, int]:
     """Synchronises the stream and returns (status, device error word)."""
     w = ctypes.c_int32(0)

@@ -55,6 +55,7 @@ SIGNATURES: dict[str, tuple] = {
     "ec_entropy_decode_workspace_size": (_sz, [_i32, _i32, _i32]),
     "ec_entropy_decode": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_entropy_decode_noalloc": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p]),
+    "ec_selftest_bounded_wait": (_i32, [_p, ctypes.c_uint64, _p]),
     "ec_lm_head_entropy_workspace_size": (_sz, [_i32]),
     "ec_lm_head_entropy": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_select_recompute": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _p, _p, _p]),

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "ec_common.cuh"
 #include "ec_internal.h"
 #include "entropycache.h"
 
@@ -86,6 +87,18 @@ StepLayout step_layout(const ec_params& p) {
   return s;
 }
 
+// One CTA: thread 0 waits for a phase of a barrier on which nothing ever arrives.
+__global__ void selftest_wait_kernel(int32_t* dev_err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    abort = 0;
+    ec::mbar_init(&bar, 1);
+    ec::fence_mbar_init();
+    ec::mbar_wait_bounded(&bar, 0, &abort, dev_err, limit_ns);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -114,6 +127,12 @@ ec_status ec_read_device_error(const int32_t* dev_err, int32_t* host_word, ec_st
   if (host_word != nullptr) *host_word = w;
   if (w == 0) return EC_OK;
   return (w & EC_DEVERR_TIMEOUT) ? EC_ERR_TIMEOUT : EC_ERR_DEVICE_CHECK;
+}
+
+ec_status ec_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, ec_stream_t stream) {
+  if (dev_err == nullptr || limit_ns < 1 || limit_ns > 10000000000ull) return EC_ERR_INVALID_ARG;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_err, limit_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 // ---- (a) ----------------------------------------------------------------------------------

@@ -126,6 +126,15 @@ const char* ec_status_string(ec_status st);
  * else EC_ERR_DEVICE_CHECK. Does not clear the word. */
 ec_status ec_read_device_error(const int32_t* dev_err, int32_t* host_word, ec_stream_t stream);
 
+/* Self-test of the failure path (the pages have no counterpart: it checks the library's own
+ * timeout handling). Launches one CTA that waits, through the same bounded mbarrier wait every
+ * kernel of the library uses, for a barrier phase that nothing completes. After limit_ns
+ * nanoseconds (1 .. 10^10) the wait gives up, ORs EC_DEVERR_TIMEOUT into *dev_err and the
+ * kernel returns normally; no asynchronous copy or tensor-core work is in flight, so the
+ * context stays usable. ec_read_device_error() then reports EC_ERR_TIMEOUT.
+ * EC_ERR_INVALID_ARG for a NULL dev_err or a limit out of range. */
+ec_status ec_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, ec_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t ec_version(void);
 

@@ -190,3 +190,11 @@ def test_lm_head_entropy_validation(capi):
     assert call(hidden=None) == INV
     assert call(weight=p + 8) == INV  # not 16-byte aligned
     assert call(ws_bytes=ws - 1) == INV
+
+
+def test_selftest_bounded_wait_validation(capi):
+    lib = capi.load()
+    INV = capi.EC_ERR_INVALID_ARG
+    assert lib.ec_selftest_bounded_wait(None, 1000, None) == INV
+    assert lib.ec_selftest_bounded_wait(1 << 20, 0, None) == INV
+    assert lib.ec_selftest_bounded_wait(1 << 20, 10 ** 10 + 1, None) == INV

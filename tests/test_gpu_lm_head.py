@@ -58,6 +58,7 @@ def run_case(E, h_bits, w_bits):
     (5, 128, 1000, 2),       # few rows (N padded to 32), ragged last vocabulary tile
     (32, 1024, 50257, 8),    # GPT-2-sized vocabulary, ragged
     (40, 512, 8192, 4),      # two 32-candidate chunks
+    (64, 128, 777, 4),       # seven vocabulary tiles over few CTAs, the last one ragged
     (256, 256, 3000, 16),    # the most rows (N = 256, eight chunks)
 ])
 def test_matches_oracle(E, n_rows, d_model, V, peaked):

@@ -49,7 +49,7 @@ extern "C" {
 typedef int32_t ec_status;
 #define EC_OK 0
 #define EC_ERR_INVALID_ARG 1   /* a null pointer, a bad size, a misaligned pointer       */
-#define EC_ERR_UNSUPPORTED 2   /* a valid request this build does not implement          */
+#define EC_ERR_UNSUPPORTED 2   /* a valid request the library does not implement          */
 #define EC_ERR_CUDA 3          /* a CUDA runtime/driver call failed                      */
 #define EC_ERR_DEVICE_CHECK 4  /* a device-side bounds/consistency check fired           */
 #define EC_ERR_TIMEOUT 5       /* a bounded device-side wait gave up                     */

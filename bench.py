@@ -111,7 +111,7 @@ def profiled_traffic(kernel: str, source: str) -> float | None:
         return None
 
 
-def run_profile(steps: int, workload: int = WORKLOAD) -> None:
+def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) -> None:
     """A few eager steps of the workload (no graphs, no timing), then as many calls of the
     standalone decode entry on the step's logits and of the output projection fused with the
     decode: a short program for ncu."""
@@ -122,8 +122,8 @@ def run_profile(steps: int, workload: int = WORKLOAD) -> None:
 
     B.build()
     w = W.workload(workload)
-    p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
-                 logits_dtype=w.logits_dtype)
+    p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec,
+                 tau=w.tau if tau is None else tau, logits_dtype=w.logits_dtype)
     st_h = W.snapshot_state(w)
     lay = W.layer_tensors(w, 0)
 
@@ -744,7 +744,7 @@ def main():
                     help="run this many eager steps and exit (a short program for ncu)")
     args = ap.parse_args()
     if args.profile_steps > 0:
-        run_profile(args.profile_steps, args.workload)
+        run_profile(args.profile_steps, args.workload, args.tau)
         return
     if args.warmup < 3:
         args.warmup = 3

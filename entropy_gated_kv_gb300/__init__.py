@@ -82,10 +82,11 @@ class Params:
     n_dec: int = 1
     tau: float = 1.0
     logits_dtype: object = "bf16"
+    conf_threshold: float = 0.0  # > 0: commit only candidates at least this confident (at least one)
 
     def c(self) -> C.EcParams:
         return C.EcParams(self.B, self.L, self.Hq, self.Hkv, self.D, self.V, self.C_max, self.k, self.n_dec,
-                          float(self.tau), _dtype_code(self.logits_dtype))
+                          float(self.tau), _dtype_code(self.logits_dtype), float(self.conf_threshold))
 
 
 class DecodeState:

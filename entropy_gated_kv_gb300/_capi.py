@@ -37,6 +37,7 @@ class EcParams(ctypes.Structure):
     _fields_ = [
         ("B", _i32), ("L", _i32), ("Hq", _i32), ("Hkv", _i32), ("D", _i32), ("V", _i32),
         ("C_max", _i32), ("k", _i32), ("n_dec", _i32), ("tau", _f32), ("logits_dtype", _i32),
+        ("conf_threshold", _f32),
     ]
 
 

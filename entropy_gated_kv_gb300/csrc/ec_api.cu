@@ -39,6 +39,7 @@ ec_status check_params(const ec_params* p, int what) {
     if (p->k < 1 || p->k > p->L) return EC_ERR_INVALID_ARG;
     if (p->n_dec < 1 || p->n_dec > p->C_max) return EC_ERR_INVALID_ARG;
     if (p->tau != p->tau) return EC_ERR_INVALID_ARG;  // NaN threshold
+    if (!(p->conf_threshold <= 1.f)) return EC_ERR_INVALID_ARG;  // NaN, or above any probability
   }
   if (what & kCheckAttn) {
     if (p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0) return EC_ERR_INVALID_ARG;

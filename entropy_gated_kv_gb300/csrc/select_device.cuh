@@ -27,6 +27,8 @@ namespace ec {
 struct SelArgs {
   int32_t L, C_max, k, n_dec;
   float tau;
+  // confidence-threshold commit: ln(conf_threshold), or -inf for the fixed-count commit
+  float log_thresh;
   const int32_t* cand_pos;
   const int32_t* cand_count;
   const int32_t* ids;
@@ -303,7 +305,10 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
       ok = ok && (__ffs(same) - 1 == lane);  // first listing of its position
       if (in && !ok) report_error(a.dev_err, EC_DEVERR_BAD_CAND_POS);
       const unsigned vmask = __ballot_sync(0xffffffffu, ok);
-      const int nD = min(n_dec, __popc(vmask));
+      const int n_above = __popc(__ballot_sync(0xffffffffu, ok && c >= a.log_thresh));
+      // the most confident candidates rank first, so the top nD are exactly those above the
+      // threshold (at least one when any candidate is valid)
+      const int nD = vmask == 0u ? 0 : min(n_dec, max(1, n_above));
       bool chosen = false;  // D: nD rounds of a warp argmax over the remaining valid candidates
       for (int r = 0; r < nD; ++r)
         if (sel_warp_best(c, p, ok && !chosen, lane) == lane) chosen = true;
@@ -372,7 +377,7 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
       }
     }
   } else {
-    int nvalid_local = 0;
+    int nvalid_local = 0;  // valid candidates, plus (<< 16) those at or above the threshold
     for (int i = tid; i < count; i += NT) {
       const int p = s_pos[i];
       bool ok = p >= 0 && sel_bit(bitmap, p);
@@ -380,9 +385,11 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
         if (s_pos[j] == p) ok = false;  // a position listed twice keeps its first occurrence
       if (!ok) report_error(a.dev_err, EC_DEVERR_BAD_CAND_POS);
       s_valid[i] = ok ? 1 : 0;
-      nvalid_local += ok ? 1 : 0;
+      nvalid_local += ok ? (s_conf[i] >= a.log_thresh ? 0x10001 : 1) : 0;
     }
-    const int nD = min(n_dec, sel_block_sum<NT>(nvalid_local, h));  // contains __syncthreads
+    const int packed = sel_block_sum<NT>(nvalid_local, h);  // contains __syncthreads
+    const int n_valid = packed & 0xFFFF, n_above = packed >> 16;
+    const int nD = n_valid == 0 ? 0 : min(n_dec, max(1, n_above));
     for (int i = tid; i < count; i += NT) {
       int rank = 0;
       if (s_valid[i]) {

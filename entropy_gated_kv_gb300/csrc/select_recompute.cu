@@ -1,6 +1,8 @@
 // select_recompute.cu — stages (b) and (c) of the EntropyCache step as a kernel of their own
 // (ec_select_recompute, and inside ec_step): one CTA per sequence runs select_prefetch and
 // select_finish (select_device.cuh).
+#include <cmath>
+
 #include "ec_internal.h"
 #include "select_device.cuh"
 
@@ -37,6 +39,7 @@ SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* can
   a.k = p.k;
   a.n_dec = p.n_dec;
   a.tau = p.tau;
+  a.log_thresh = p.conf_threshold > 0.f ? logf(p.conf_threshold) : -INFINITY;
   a.cand_pos = cand_pos;
   a.cand_count = cand_count;
   a.ids = ids;

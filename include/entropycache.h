@@ -77,15 +77,22 @@ typedef void* ec_stream_t; /* a cudaStream_t */
  *        logits the step receives (1 <= C_max <= min(L, 1024))
  * k      decode-history length: how many of the most recently decoded positions a
  *        partial step recomputes (1 <= k <= L)
- * n_dec  tokens committed per sequence per step (1 <= n_dec <= C_max)
+ * n_dec  tokens committed per sequence per step (1 <= n_dec <= C_max): the n_dec most
+ *        confident candidates
  * tau    entropy threshold in nats: a step whose decoded tokens' maximum entropy is
  *        strictly above tau triggers a full recompute
  * logits_dtype  EC_F32 or EC_BF16
+ * conf_threshold  0 (or less): commit the n_dec most confident candidates. Greater than 0
+ *        (at most 1): a confidence-threshold commit, a decoding variant that the pages leave
+ *        open — of those n_dec, only the candidates whose decode confidence p(id) is at least
+ *        conf_threshold are committed, and the single most confident one when none is. A
+ *        zero-initialised struct gets the fixed-count commit.
  */
 typedef struct ec_params {
   int32_t B, L, Hq, Hkv, D, V, C_max, k, n_dec;
   float tau;
   int32_t logits_dtype;
+  float conf_threshold;
 } ec_params;
 
 /* ---- per-sequence decode state (all device arrays, caller-owned) ----------------------

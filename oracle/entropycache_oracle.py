@@ -116,21 +116,27 @@ def lm_head_entropy(hidden: np.ndarray, weight: np.ndarray) -> tuple[np.ndarray,
 # (b) the decoded set and the max-entropy gate  —  [zh] §2.2, [pt] §2 "Decisão de Pulo"
 
 
-def select_decoded(cand_pos: np.ndarray, count: int, log_conf: np.ndarray, n_dec: int) -> list[int]:
+def select_decoded(cand_pos: np.ndarray, count: int, log_conf: np.ndarray, n_dec: int,
+                   conf_threshold: float = 0.0) -> list[int]:
     """Candidate rows committed this step: the n_dec most confident among the first `count`.
 
     Ranking key: higher log_conf first (NaN ranks lowest), then the smaller position.
-    Returns candidate row numbers sorted by ascending position.
+    With conf_threshold > 0 (a confidence-threshold commit, a decoding variant) only those of
+    them whose confidence p = exp(log_conf) is at least the threshold are committed, and the
+    single most confident one when none is. Returns candidate row numbers sorted by ascending
+    position.
     """
 
-    def key(i: int) -> tuple[float, int]:
+    def eff(i: int) -> float:
         c = float(log_conf[i])
-        if math.isnan(c):
-            c = -math.inf
-        return (-c, int(cand_pos[i]))
+        return -math.inf if math.isnan(c) else c
 
-    order = sorted(range(int(count)), key=key)
+    order = sorted(range(int(count)), key=lambda i: (-eff(i), int(cand_pos[i])))
     chosen = order[: int(n_dec)]
+    if conf_threshold > 0.0 and chosen:
+        lt = math.log(conf_threshold)
+        above = [i for i in chosen if eff(i) >= lt]
+        chosen = above if above else chosen[:1]
     return sorted(chosen, key=lambda i: int(cand_pos[i]))
 
 
@@ -246,6 +252,7 @@ def step(
     ring_count: int,
     n_dec: int,
     tau: float,
+    conf_threshold: float = 0.0,
     layers: list[dict] | None = None,
     scale: float | None = None,
     attention_rows: np.ndarray | None = None,
@@ -262,7 +269,7 @@ def step(
     C = int(cand_count)
     ids, ent, conf = entropy_decode(logits[:C]) if C > 0 else (
         np.zeros(0, np.int64), np.zeros(0), np.zeros(0))
-    rows = select_decoded(cand_pos, C, conf, n_dec)
+    rows = select_decoded(cand_pos, C, conf, n_dec, conf_threshold)
     tokens = np.array(tokens, dtype=np.int64, copy=True)
     mask = np.array(mask, dtype=np.uint8, copy=True)
     for i in rows:

@@ -198,3 +198,16 @@ def test_selftest_bounded_wait_validation(capi):
     assert lib.ec_selftest_bounded_wait(None, 1000, None) == INV
     assert lib.ec_selftest_bounded_wait(1 << 20, 0, None) == INV
     assert lib.ec_selftest_bounded_wait(1 << 20, 10 ** 10 + 1, None) == INV
+
+
+def test_conf_threshold_validation(capi):
+    import math
+
+    lib = capi.load()
+    # the step's workspace query validates every parameter: 0 marks a rejected set
+    for ok in (0.0, -1.0, 0.5, 1.0):
+        p = _params(capi, conf_threshold=ok)
+        assert lib.ec_step_workspace_size(ctypes.byref(p)) > 0, ok
+    for bad in (math.nan, 1.5):
+        p = _params(capi, conf_threshold=bad)
+        assert lib.ec_step_workspace_size(ctypes.byref(p)) == 0, bad

@@ -51,13 +51,13 @@ def make_case(rng, B, L, C_max, k, n_dec, tau):
                 ring_count=count, ids=ids, ent=ent, conf=conf)
 
 
-def oracle_select(c, b, C_max, n_dec, tau, L):
+def oracle_select(c, b, C_max, n_dec, tau, L, gamma=0.0):
     rows = slice(b * C_max, (b + 1) * C_max)
     cp = c["cand_pos"][b]
     cnt = int(c["cand_count"][b])
     conf = c["conf"][rows].astype(np.float64)
     ent = c["ent"][rows].astype(np.float64)
-    dec = O.select_decoded(cp, cnt, conf, n_dec)
+    dec = O.select_decoded(cp, cnt, conf, n_dec, gamma)
     tokens = c["tokens"][b].astype(np.int64).copy()
     mask = c["mask"][b].copy()
     for i in dec:
@@ -72,6 +72,10 @@ def oracle_select(c, b, C_max, n_dec, tau, L):
                 ring_head=head, ring_count=count, idx=idx)
 
 
+# gamma: the confidence-threshold commit (0 = the n_dec most confident). The generated
+# log-confidences lie on a grid of 0.5 (0, -0.5, -1, -1.5), so ln(gamma) is well clear of every
+# value: -0.75 between grid points, and ln(0.999) just below 0 (only certain candidates pass).
+@pytest.mark.parametrize("gamma", [0.0, float(np.exp(-0.75)), 0.999])
 @pytest.mark.parametrize("seed,B,L,C_max,k,n_dec,tau", [
     (0, 4, 16, 8, 4, 1, 1.0),
     (1, 8, 64, 16, 8, 3, 0.75),
@@ -81,12 +85,13 @@ def oracle_select(c, b, C_max, n_dec, tau, L):
     (5, 1, 32768, 32, 64, 1, 1.0),
     (6, 2, 12, 12, 12, 12, 0.0),
 ])
-def test_select_recompute_matches_oracle(E, seed, B, L, C_max, k, n_dec, tau):
+def test_select_recompute_matches_oracle(E, seed, B, L, C_max, k, n_dec, tau, gamma):
     import torch
 
     rng = np.random.default_rng(seed)
     c = make_case(rng, B, L, C_max, k, n_dec, tau)
-    p = E.Params(B=B, L=L, Hq=1, Hkv=1, D=64, V=50000, C_max=C_max, k=k, n_dec=n_dec, tau=tau)
+    p = E.Params(B=B, L=L, Hq=1, Hkv=1, D=64, V=50000, C_max=C_max, k=k, n_dec=n_dec, tau=tau,
+                 conf_threshold=gamma)
     st = E.DecodeState.from_arrays(p, tokens=c["tokens"], mask=c["mask"], ring=c["ring"], ring_head=c["ring_head"],
                                    ring_count=c["ring_count"])
     E.select_recompute(p, st, to_dev(c["cand_pos"]), to_dev(c["cand_count"]), to_dev(c["ids"]), to_dev(c["ent"]),
@@ -95,7 +100,7 @@ def test_select_recompute_matches_oracle(E, seed, B, L, C_max, k, n_dec, tau):
     got = {f: getattr(st, f).cpu().numpy() for f in st.FIELDS}
     assert got["dev_err"][0] == 0
     for b in range(B):
-        o = oracle_select(c, b, C_max, n_dec, tau, L)
+        o = oracle_select(c, b, C_max, n_dec, tau, L, gamma)
         np.testing.assert_array_equal(got["tokens"][b], o["tokens"])
         np.testing.assert_array_equal(got["mask"][b], o["mask"])
         nd = len(o["dec_pos"])

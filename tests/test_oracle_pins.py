@@ -375,3 +375,19 @@ def test_lm_head_entropy_brute_force_dot_products():
         np.testing.assert_array_equal(got[0], want[0])
         np.testing.assert_allclose(got[1], want[1], rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(got[2], want[2], rtol=1e-12, atol=1e-14)
+
+
+def test_confidence_threshold_commit_by_hand():
+    # confidences .9, .6, .3, .8 at positions 10..13, n_dec = 3: the three most confident are
+    # rows 0 (.9), 3 (.8), 1 (.6)
+    pos = np.array([10, 11, 12, 13])
+    lc = np.log(np.array([0.9, 0.6, 0.3, 0.8]))
+    assert O.select_decoded(pos, 4, lc, 3) == [0, 1, 3]
+    assert O.select_decoded(pos, 4, lc, 3, conf_threshold=0.7) == [0, 3]  # .9 and .8 pass
+    assert O.select_decoded(pos, 4, lc, 3, conf_threshold=0.6) == [0, 1, 3]  # >= includes .6
+    assert O.select_decoded(pos, 4, lc, 3, conf_threshold=0.95) == [0]  # none: the best one
+    assert O.select_decoded(pos, 4, lc, 1, conf_threshold=0.5) == [0]  # n_dec still caps
+    assert O.select_decoded(pos, 0, lc, 3, conf_threshold=0.5) == []  # nothing to commit
+    # NaN confidence never passes and ranks last
+    lc2 = np.array([math.nan, math.log(0.8), math.log(0.2)])
+    assert O.select_decoded(pos[:3], 3, lc2, 3, conf_threshold=0.5) == [1]

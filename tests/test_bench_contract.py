@@ -1,0 +1,70 @@
+"""The bench's JSON line, built from a synthetic measurement on the CPU: every key of the
+contract is present, and the derived numbers (whole-job steps/s, per-step time, the roofline's
+achieved rate and fraction, the launch count) follow from the inputs by the stated formulas."""
+import argparse
+import json
+
+import pytest
+
+import bench
+
+
+def _args(**kw):
+    a = dict(steps=1000, warmup=5, workload=bench.WORKLOAD, tau=None, no_cpu_baseline=True, cpu_seconds=1.0)
+    a.update(kw)
+    return argparse.Namespace(**a)
+
+
+def _res(ms=25.0, attn_us=9.0, ent_us=6.0):
+    return {
+        "ms": ms,
+        "kernels": {"R": 95, "entropy_decode_us": ent_us, "partial_attention_us": attn_us, "kv_scatter_us": 2.0},
+        "flag": False,
+        "R": 95,
+        "copy_mb": 58.0,
+        "e2e": {"value": 5000.0, "unit": "steps/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 2},
+        "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
+    }
+
+
+def _line(capsys, args, res, world=1):
+    bench.emit_ours(args, res, 0, world)
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1, out  # exactly one JSON line
+    return json.loads(out[0])
+
+
+def test_every_contract_key_and_derived_value(capsys):
+    line = _line(capsys, _args(), _res())
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["metric"] == bench.METRIC
+    assert line["value"] == pytest.approx(1000 / 0.025)  # whole-job steps per second
+    assert line["ms_per_step"] == pytest.approx(0.025)
+    assert (line["unit"], line["n_gpus"], line["steps"], line["warmup"]) == ("steps/s", 1, 1000, 5)
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["vs_baseline"] is None
+    assert line["data"] == "synthetic" and "workload" in line["config"]
+    assert line["gpu_launches"] == 4 * 1000  # the step's four kernels per timed step
+    assert line["e2e"]["value"] == 5000.0 and line["clocks"]["sm_mhz"] == 2070.0
+
+
+def test_roofline_is_the_slowest_stage_against_its_bound(capsys):
+    line = _line(capsys, _args(), _res(attn_us=9.0, ent_us=6.0))
+    roof = line["roofline"]
+    assert roof["kernel"] == "partial_attention"  # the larger per-step time
+    assert roof["bound"] == "hbm"  # 87 flops per byte at R = 95, below the ridge
+    alg = bench.algorithmic(bench.bench_workload(_args()), 95)
+    assert roof["achieved"] == pytest.approx(alg["partial_attention_bytes"] / 9e-6 / 1e9)
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in roof
+    # when the decode stage is the slower one it becomes the reported kernel
+    line = _line(capsys, _args(), _res(attn_us=5.0, ent_us=6.0))
+    assert line["roofline"]["kernel"] == "entropy_decode" and line["roofline"]["unit"] == "GB/s"
+
+
+def test_whole_job_value_scales_with_ranks(capsys):
+    line = _line(capsys, _args(), _res(), world=2)
+    assert line["n_gpus"] == 2
+    assert line["value"] == pytest.approx(2 * 1000 / 0.025)  # every rank's steps over the slowest rank's time

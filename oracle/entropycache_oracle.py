@@ -21,6 +21,8 @@ Readings where the pages are silent (each also listed in the design notes):
   - "decode" is greedy argmax, ties to the lowest vocabulary index;
   - the tokens decoded in a step (the set D) are the n_dec candidates with the highest
     confidence p(argmax), ties to the lower position; a NaN confidence ranks lowest;
+    optionally (a confidence-threshold commit, one of the decoding strategies the gate carries
+    over to: [pt] §5, [zh] §5) only those with p >= conf_threshold, at least one;
   - an empty D gives E = 0 (partial); a NaN E gives a full step; E == tau is partial;
   - the history pushes D in ascending position order and survives full steps;
   - attention is unmasked (bidirectional) with scale 1/sqrt(D) by default, query head h

@@ -68,3 +68,33 @@ def test_whole_job_value_scales_with_ranks(capsys):
     line = _line(capsys, _args(), _res(), world=2)
     assert line["n_gpus"] == 2
     assert line["value"] == pytest.approx(2 * 1000 / 0.025)  # every rank's steps over the slowest rank's time
+
+
+def test_flat_state_layout():
+    # the e2e loop restores the decode state with one copy and reads E, flag and R back as one
+    # slice: every field must be a view of the flat buffer, naturally aligned, the mask 16-byte
+    # aligned (the library reads it with 16-byte loads), and E, flag, R adjacent in that order
+    import numpy as np
+    import torch
+
+    import entropy_gated_kv_gb300 as E
+
+    p = E.Params(B=3, L=40, Hq=1, Hkv=1, D=64, V=100, C_max=4, k=5, n_dec=2)
+    tokens = np.arange(120).reshape(3, 40)
+    st, flat, (r0, r1) = bench.flat_state(E, p, "cpu", tokens=tokens, mask=np.ones((3, 40)))
+    base = flat.data_ptr()
+    for f in E.DecodeState.FIELDS:
+        t = getattr(st, f)
+        off = t.data_ptr() - base
+        assert 0 <= off and off + t.numel() * t.element_size() <= flat.numel(), f
+        assert off % (16 if f == "mask" else t.element_size()) == 0, f
+    assert st.flag.dtype == torch.uint8 and tuple(st.flag.shape) == (3,)
+    assert st.E.data_ptr() - base == r0 and st.R.data_ptr() - base + 3 * 4 == r1
+    np.testing.assert_array_equal(st.tokens.numpy(), tokens)
+    st.E.fill_(0.5)
+    st.flag.fill_(1)
+    st.R.fill_(7)
+    blob = flat[r0:r1].clone()
+    assert blob[:12].view(torch.float32).tolist() == [0.5] * 3
+    assert blob[12:15].tolist() == [1, 1, 1]
+    assert blob[-12:].view(torch.int32).tolist() == [7] * 3

@@ -98,3 +98,25 @@ def test_flat_state_layout():
     assert blob[:12].view(torch.float32).tolist() == [0.5] * 3
     assert blob[12:15].tolist() == [1, 1, 1]
     assert blob[-12:].view(torch.int32).tolist() == [7] * 3
+
+
+def test_reference_arm_line():
+    # the oracle arm runs on the host cores: one JSON line with the same metric, unit and
+    # direction as ours, marked impl = reference, its e2e equal to its own value with no copies
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "steps/s" and d["higher_is_better"] is True and d["warmup"] >= 3
+    assert d["value"] > 0 and d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]

@@ -18,6 +18,11 @@
  *                                                  -> ec_partial_attention
  *   ec_step runs (a)(b)(c) once and then (c-scatter)(d) for every layer.
  *
+ * Beyond the step: ec_lm_head_entropy computes (a) from the candidates' hidden states (the
+ * output projection fused with the decode, so the logits are never stored);
+ * ec_entropy_decode_noalloc is (a) for callers that cannot allocate a workspace; and
+ * ec_selftest_bounded_wait exercises the kernels' timeout path.
+ *
  * Conventions shared by every entry point
  *   - Every call returns an ec_status and never throws or aborts.
  *   - Every data pointer is a DEVICE pointer owned by the caller (allocated by any means,

@@ -630,17 +630,8 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
     *status = EC_ERR_INVALID_ARG;
     return cudaErrorInvalidValue;
   }
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) {
-    *status = EC_ERR_CUDA;
-    return e;
-  }
   // Clusters of kCluster CTAs, one CTA per SM (shared memory bound), as many clusters as
-  // fit on the device at once (the kernel is persistent).
-  static int max_clusters[2] = {0, 0};  // per head size
-  int& mc = max_clusters[D == 128 ? 1 : 0];
+  // fit on the device at once (the kernel is persistent); counted once per device and head size.
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -654,20 +645,28 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
-  if (mc == 0) {
-    e = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kDynSmem);
-    if (e != cudaSuccess) {
-      *status = EC_ERR_CUDA;
-      return e;
-    }
-    cfg.gridDim = dim3(std::min(sms, kMaxGrid) / kCluster * kCluster);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, attention_kernel<D>, &cfg);
-    if (e != cudaSuccess || n < 1) {
-      *status = EC_ERR_CUDA;
-      return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-    }
-    mc = std::min(n, kMaxGrid / kCluster);
+  int mc = 0;
+  cudaError_t e = cached_per_device(
+      D, &mc,
+      [](int* n_out, void* ctx) -> cudaError_t {
+        cudaLaunchConfig_t* c = static_cast<cudaLaunchConfig_t*>(ctx);
+        int sms = 0;
+        cudaError_t r = current_device_sms(&sms);
+        if (r == cudaSuccess)
+          r = cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kDynSmem);
+        if (r != cudaSuccess) return r;
+        c->gridDim = dim3(std::min(sms, kMaxGrid) / kCluster * kCluster);
+        int n = 0;
+        r = cudaOccupancyMaxActiveClusters(&n, attention_kernel<D>, c);
+        if (r != cudaSuccess) return r;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        *n_out = std::min(n, kMaxGrid / kCluster);
+        return cudaSuccess;
+      },
+      &cfg);
+  if (e != cudaSuccess) {
+    *status = EC_ERR_CUDA;
+    return e;
   }
   cfg.gridDim = dim3(mc * kCluster);
   cfg.numAttrs = 2;

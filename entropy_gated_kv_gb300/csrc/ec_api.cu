@@ -6,10 +6,61 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "ec_common.cuh"
 #include "ec_internal.h"
 #include "entropycache.h"
+
+namespace ec {
+
+static std::mutex g_cfg_mutex;
+static std::map<std::pair<int, const void*>, size_t> g_dyn_smem;  // (device, kernel) -> configured bytes
+static std::map<std::pair<int, int>, int> g_cached;               // (device, key) -> value
+
+cudaError_t current_device_sms(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  size_t& have = g_dyn_smem[{dev, func}];
+  if (bytes <= have) return cudaSuccess;
+  if (bytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+  }
+  have = bytes;
+  return cudaSuccess;
+}
+
+cudaError_t cached_per_device(int key, int* value, cudaError_t (*make)(int* value, void* ctx), void* ctx) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  auto it = g_cached.find({dev, key});
+  if (it != g_cached.end()) {
+    *value = it->second;
+    return cudaSuccess;
+  }
+  int v = 0;
+  e = make(&v, ctx);
+  if (e != cudaSuccess) return e;
+  g_cached[{dev, key}] = v;
+  *value = v;
+  return cudaSuccess;
+}
+
+}  // namespace ec
 
 using namespace ec;
 

@@ -74,6 +74,18 @@ cudaError_t launch_partial_attention(const ec_params& p, const void* q, const vo
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// ---- per-device launch configuration (ec_api.cu) -------------------------------------------
+// Kernel attributes and device properties apply per device, and the entry points may be
+// called from several host threads and on several devices, so every cached value is kept
+// per device behind a lock.
+// SM count of the current device.
+cudaError_t current_device_sms(int* sms);
+// Raises `func`'s dynamic shared-memory limit on the current device to at least `bytes`.
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
+// A value computed once per (current device, key) by `make` (which returns cudaSuccess and
+// sets *value, or an error that is returned and not cached).
+cudaError_t cached_per_device(int key, int* value, cudaError_t (*make)(int* value, void* ctx), void* ctx);
+
 }  // namespace ec
 
 namespace ec {

@@ -826,13 +826,8 @@ int32_t entropy_num_chunks(int32_t V, int32_t dtype) {
 
 template <int DT>
 cudaError_t launch_stream(int grid, cudaStream_t s, const EntArgs& a) {
-  static bool configured = false;
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(entropy_stream_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(stream_smem_bytes<DT>()));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(entropy_stream_kernel<DT>), stream_smem_bytes<DT>());
+  if (e != cudaSuccess) return e;
   return launch_pdl(entropy_stream_kernel<DT>, dim3(grid), dim3(kStreamThreads), stream_smem_bytes<DT>(), s, a);
 }
 
@@ -858,9 +853,8 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
             static_cast<ChunkPartial*>(ws),
             reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + align_up(rows * nch * sizeof(ChunkPartial), 256)),
             publish_only ? 1 : 0, row_count, rows_per_group, n_rows, dev_err};
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  const cudaError_t e = current_device_sms(&sms);
   if (e != cudaSuccess) return e;
   const int64_t total_bytes = static_cast<int64_t>(n_rows) * V * (f32 ? 4 : 2);
   // not in publish-only mode (inside a step): the persistent CTAs cannot start beside the

@@ -89,12 +89,9 @@ cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, 
   // one CTA per recompute row, at most two per SM in total so the whole grid is resident at
   // once (the next kernel can then launch early); R lives on the device, so CTAs stride over
   // the rows
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
+  int sms = 0;
+  const cudaError_t e = current_device_sms(&sms);
+  if (e != cudaSuccess) return e;
   const int64_t cap = std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / p.B);
   const int gx = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.L, cap)));
   const dim3 grid(gx, p.B);

@@ -66,13 +66,8 @@ cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, cons
                                     const float* log_conf, bool prefetch_early, const ChunkPartial* partials,
                                     int32_t nchunks, cudaStream_t s) {
   const size_t smem = select_smem_bytes(p);
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(select_recompute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(select_recompute_kernel), smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(select_recompute_kernel, dim3(p.B), dim3(kThreads), smem, s,
                     make_sel_args(p, st, cand_pos, cand_count, ids, entropy, log_conf, prefetch_early, partials,
                                   nchunks));

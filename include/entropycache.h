@@ -186,7 +186,9 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
  * e.g. more than about 4000 rows of a 126464-entry bf16 vocabulary) returns
  * EC_ERR_UNSUPPORTED and launches nothing.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current): make that first call before any stream capture.
+ * with that device current): make that first call before any stream capture. The address is
+ * kept for the life of the process; cudaDeviceReset() on a device invalidates it, so do not
+ * call this entry point on a device after resetting it.
  * Every call shares the one array, which keeps the last call's contents; each call clears the
  * counters it needs with an asynchronous memset on `stream` before its kernel. Calls whose
  * executions overlap on the GPU (other streams, other host threads) race and give wrong

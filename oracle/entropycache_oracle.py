@@ -258,6 +258,7 @@ def step(
     layers: list[dict] | None = None,
     scale: float | None = None,
     attention_rows: np.ndarray | None = None,
+    decoded_rows: list[int] | None = None,
 ) -> dict:
     """One denoising step of one sequence.
 
@@ -266,12 +267,18 @@ def step(
     k_cache, v_cache [L, Hkv, D], k_src, v_src [L, Hkv, D] (fresh rows by position) and
     q_src [L, Hq, D] (queries by position). attention_rows optionally restricts which
     recompute rows get an attention output (a sample); None computes all of them.
+    decoded_rows optionally fixes the committed candidate rows instead of ranking them: a
+    checker that finds two candidates' confidences tied within rounding adopts the device's
+    choice among them this way, then checks everything that follows from it.
     Returns decode results, the gate, the new state, idx and per-layer outputs.
     """
     C = int(cand_count)
     ids, ent, conf = entropy_decode(logits[:C]) if C > 0 else (
         np.zeros(0, np.int64), np.zeros(0), np.zeros(0))
-    rows = select_decoded(cand_pos, C, conf, n_dec, conf_threshold)
+    if decoded_rows is None:
+        rows = select_decoded(cand_pos, C, conf, n_dec, conf_threshold)
+    else:
+        rows = sorted((int(i) for i in decoded_rows), key=lambda i: int(cand_pos[i]))
     tokens = np.array(tokens, dtype=np.int64, copy=True)
     mask = np.array(mask, dtype=np.uint8, copy=True)
     for i in rows:

@@ -4,7 +4,9 @@ refreshed caches bit for bit; E within 1e-3; attention within the bf16 tolerance
 
 Exemptions (the fp32 kernel and the fp64 oracle may round a near-tie differently):
   - a sequence's flag, and the recompute set that depends on it, when |E_oracle - tau| <= 1e-4;
-  - the committed set when the oracle's n_dec-th and next confidence differ by <= 1e-5.
+  - the committed set when the oracle's n_dec-th and next confidence differ by <= 1e-5: the
+    device's choice must lie in the tied band, and the oracle then adopts it (teacher forcing)
+    so that the mask, history, gate, recompute set, caches and attention are still checked.
 Each exemption is reported; the seeded workloads hit none of them.
 """
 import math
@@ -58,9 +60,21 @@ def run_and_check(E, w, st_h, lg, lay, sample_rows=None, seed=0):
                    mask=st_h["mask"][b], ring=st_h["ring"][b], ring_head=int(st_h["ring_head"][b]),
                    ring_count=int(st_h["ring_count"][b]), n_dec=w.n_dec, tau=w.tau)
         conf_sorted = sorted(o["log_conf"][:cnt], reverse=True)
+        gpu_dec = [int(x) for x in g["dec_pos"][b] if x >= 0]
         if cnt > w.n_dec and conf_sorted[w.n_dec - 1] - conf_sorted[w.n_dec] <= 1e-5:
-            pytest.skip(f"b={b}: commit near-tie exemption")
-        assert g["dec_pos"][b, : len(o["dec_pos"])].tolist() == o["dec_pos"]
+            # commit near-tie: the device ranks fp32 confidences, the oracle fp64. The device's
+            # choice must be n_dec candidates from the top of the ranking (each within 1e-5 of
+            # the n_dec-th confidence or above it); the oracle then adopts that choice and
+            # everything that follows from it is checked as usual.
+            band = conf_sorted[w.n_dec - 1] - 1e-5
+            allowed = {int(st_h["cand_pos"][b][i]) for i in range(cnt) if o["log_conf"][i] >= band}
+            assert len(gpu_dec) == w.n_dec and set(gpu_dec) <= allowed, (b, gpu_dec, sorted(allowed))
+            rows = [i for i in range(cnt) if int(st_h["cand_pos"][b][i]) in gpu_dec]
+            o = O.step(logits=x, cand_pos=st_h["cand_pos"][b], cand_count=cnt, tokens=st_h["tokens"][b],
+                       mask=st_h["mask"][b], ring=st_h["ring"][b], ring_head=int(st_h["ring_head"][b]),
+                       ring_count=int(st_h["ring_count"][b]), n_dec=w.n_dec, tau=w.tau, decoded_rows=rows)
+            print(f"b={b}: commit near-tie exemption, device chose {gpu_dec}")
+        assert gpu_dec == o["dec_pos"], (b, gpu_dec, o["dec_pos"])
         np.testing.assert_array_equal(g["tokens"][b], o["tokens"])
         np.testing.assert_array_equal(g["mask"][b], o["mask"])
         assert int(g["ring_head"][b]) == o["ring_head"] and int(g["ring_count"][b]) == o["ring_count"]
@@ -126,6 +140,23 @@ def test_mixed_flags_in_one_batch(E):
             lg[b] = rng.standard_normal((w.C_max, w.V)) * 0.5
     flags = run_and_check(E, w, st_h, W.to_bf16_bits(lg), W.layer_tensors(w, 0), sample_rows=64)
     assert flags == [False, True, False, True]
+
+
+def test_mixed_flags_at_full_dream_shape(E):
+    # The Dream-7B GQA workload at its own shape (B 8, 28 q / 4 kv heads x 128, L 2048,
+    # V 152064 bf16) with per-sequence skip flags: even sequences get a confident candidate
+    # (N(0, 1) noise plus a peak, a partial step), odd ones keep the Zipf-ranked logits of
+    # the workload (every row has entropy > 3.5: a full step).
+    w = W.workload(3)
+    st_h = W.snapshot_state(w)
+    lg = W.step_logits(w)
+    rng = np.random.default_rng(31)
+    for b in range(0, w.B, 2):
+        x = rng.standard_normal((w.C_max, w.V), dtype=np.float32)
+        x[np.arange(w.C_max), rng.integers(0, w.V, w.C_max)] += (8.0 + 0.25 * np.arange(w.C_max)).astype(np.float32)
+        lg[b] = W.to_bf16_bits(x)
+    flags = run_and_check(E, w, st_h, lg, W.layer_tensors(w, 0), sample_rows=32)
+    assert flags == [False, True] * (w.B // 2)
 
 
 def test_partial_step_with_short_history_and_ragged_candidates(E):

@@ -3,8 +3,12 @@
 Callers such as a serving runtime's custom-op interface hold only their input and output
 buffers and cannot allocate scratch; this entry point uses a library-owned static device
 array instead. The test calls it through the C ABI twice in a row and compares each result
-with the workspace entry point (ids exact, entropy and log-confidence within 1e-3, the
-tolerance of the entropy parity tests). It also checks that an oversized request is refused.
+with the float64 oracle and with the workspace entry point (ids exact, entropy and
+log-confidence within 1e-3, the tolerance of the entropy parity tests). One case takes the
+split launch, the one that keeps per-chunk partials and per-row counters in the static
+array, and calls it with two different row counts, so that the second call's counters lie
+where the first call left partial results: only the call's own clearing of its counters
+makes the second result right. It also checks that an oversized request is refused.
 
 This file is collected last, so a run that stops at the first failure has already run every
 other test; it passes alone in a fresh process too (the first call sets up the array's
@@ -15,6 +19,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle as O
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -55,24 +60,53 @@ def _compare(got, want):
     assert np.max(np.abs(got[2].astype(np.float64) - want[2])) <= ENT_TOL
 
 
-@pytest.mark.parametrize("cfg", [2, 1, 3])  # 3: 78 MB of logits, the streaming launch
-def test_noalloc_matches_workspace_entry_point_twice(env, cfg):
+def _oracle(lg_bits, dtype):
+    ids, ent, conf = O.entropy_decode(O.widen(lg_bits, dtype))
+    return ids, ent, conf
+
+
+def _device(torch, lg, dtype):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(lg).view(np.int16)).cuda().view(torch.bfloat16), 1
+    return torch.from_numpy(np.ascontiguousarray(lg)).cuda(), 0
+
+
+@pytest.mark.parametrize("cfg", [2, 1, 3])  # 2, 1: the cluster launch; 3: 78 MB, the streaming launch
+def test_noalloc_matches_oracle_and_workspace_entry_point_twice(env, cfg):
     E, torch = env
     w = W.workload(cfg)
     lg = W.step_logits(w).reshape(-1, w.V)
-    if w.logits_dtype == "bf16":
-        t = torch.from_numpy(lg.view(np.int16)).cuda().view(torch.bfloat16)
-        code = 1
-    else:
-        t = torch.from_numpy(lg).cuda()
-        code = 0
+    t, code = _device(torch, lg, w.logits_dtype)
+    want = _oracle(lg, w.logits_dtype)
     ids, ent, conf = E.entropy_decode(t)  # the existing entry point, with a workspace
     torch.cuda.synchronize()
-    want = (ids.cpu().numpy(), ent.cpu().numpy().astype(np.float64), conf.cpu().numpy().astype(np.float64))
+    ws_result = (ids.cpu().numpy(), ent.cpu().numpy().astype(np.float64), conf.cpu().numpy().astype(np.float64))
+    _compare(ws_result, want)
     first = _call_noalloc(E, t, w.V, code, t.shape[0])
     _compare(first, want)
+    _compare(first, ws_result)
     second = _call_noalloc(E, t, w.V, code, t.shape[0])  # the shared array now holds the first call's data
     _compare(second, want)
+    _compare(second, ws_result)
+
+
+def test_noalloc_split_launch_with_changing_row_counts(env):
+    # 100 and then 77 rows of a 126464-entry bf16 vocabulary: more rows than the cluster launch
+    # takes, under the streaming threshold, so both calls run the split launch with 16 chunk
+    # partials per row and one counter per row in the static array. The second call's counters
+    # start 19712 bytes in, inside the first call's partials.
+    E, torch = env
+    w = W.workload(2).scaled(B=4, seed=71)
+    lg = W.step_logits(w).reshape(-1, w.V)  # 128 rows, N(0, s^2) with s ~ U[0.5, 8]
+    for r0, n in ((0, 100), (37, 77)):
+        part = np.ascontiguousarray(lg[r0:r0 + n])
+        t, code = _device(torch, part, "bf16")
+        want = _oracle(part, "bf16")
+        got = _call_noalloc(E, t, w.V, code, n)
+        _compare(got, want)
+        ids, ent, conf = E.entropy_decode(t)
+        torch.cuda.synchronize()
+        _compare(got, (ids.cpu().numpy(), ent.cpu().numpy().astype(np.float64), conf.cpu().numpy().astype(np.float64)))
 
 
 def test_noalloc_refuses_requests_beyond_its_scratch(env):

@@ -44,6 +44,8 @@ METRIC = "EntropyCache steps/s at LLaDA-8B layer shape; % of HBM / tensor-core r
 WORKLOAD = 2
 NCOPY = 4
 CHUNK = 500
+STEADY_CHUNK = 500
+STEADY_REPEATS = 5
 
 
 # ---- multi-rank helpers (replicas: one independent step loop per rank, no data exchange) ----
@@ -234,6 +236,155 @@ def bench_workload(args):
     return w
 
 
+def params_of(E, w):
+    return E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
+                    logits_dtype=w.logits_dtype)
+
+
+def host_inputs(w, dev):
+    """The workload's own seeded inputs (the arrays the parity tests check), on the device."""
+    import torch
+
+    lg_h = W.step_logits(w)
+    lay_h = W.layer_tensors(w, 0)
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    base = {n: bf(lay_h[n]) for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
+    base["logits"] = bf(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(lg_h).to(dev)
+    return base, lg_h, lay_h
+
+
+def device_inputs(w, dev, seed, logits=None):
+    """Inputs of the workload's shapes and distributions drawn on the device (the step's time
+    depends only on shapes and on the gate, which the host-drawn logits and state decide):
+    K/V cache and queries ~ N(0, 1), fresh rows = cache + N(0, 0.05^2), all bf16."""
+    import torch
+
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    bf = torch.bfloat16
+    kv = (w.B, w.L, w.Hkv, w.D)
+    d = {}
+    for n in ("k", "v"):
+        c = torch.randn(kv, generator=g, device=dev)
+        d[f"{n}_cache"] = c.to(bf)
+        d[f"{n}_src"] = (d[f"{n}_cache"].float() + 0.05 * torch.randn(kv, generator=g, device=dev)).to(bf)
+        del c
+    d["q_src"] = torch.randn(w.B, w.L, w.Hq, w.D, generator=g, device=dev).to(bf)
+    if logits is not None:
+        d["logits"] = logits
+    return d
+
+
+def make_copies(base, w, dev, min_bytes=256 << 20, max_copies=64):
+    """Copies of the per-step inputs to rotate over, enough that one rotation (at least
+    min_bytes) exceeds the 129 MB L2, so no step finds its inputs in L2."""
+    import torch
+
+    per = sum(t.numel() * t.element_size() for t in base.values())
+    n = max(1, min(max_copies, -(-min_bytes // per)))
+    copies = []
+    for c in range(n):
+        d = {k: (t if c == 0 else t.clone()) for k, t in base.items()}
+        d["out"] = torch.zeros(w.B, w.L, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+        copies.append(d)
+    return copies, per
+
+
+class StepLoop:
+    """K steps of ec_step over rotating input copies, replayed from CUDA graphs of up to CHUNK
+    steps. Every step owns a fresh copy of the decode state, restored inside the graph."""
+
+    def __init__(self, E, p, w, copies, st_h, dev, nstate):
+        import torch
+
+        self.E, self.p, self.w, self.copies, self.dev = E, p, w, copies, dev
+        self.cand_pos = torch.from_numpy(st_h["cand_pos"]).to(dev)
+        self.cand_count = torch.from_numpy(st_h["cand_count"]).to(dev)
+        self.ws = E.workspace(E.step_workspace_size(p), dev)
+        self.pristine = E.DecodeState.from_arrays(p, device=dev, tokens=st_h["tokens"], mask=st_h["mask"],
+                                                  ring=st_h["ring"], ring_head=st_h["ring_head"],
+                                                  ring_count=st_h["ring_count"])
+        self.nstate = nstate
+        self.states = {f: getattr(self.pristine, f).unsqueeze(0).repeat(nstate, *([1] * getattr(self.pristine, f).dim()))
+                       .contiguous() for f in E.DecodeState.FIELDS}
+
+    def state(self, i):
+        s = object.__new__(self.E.DecodeState)
+        for f in self.E.DecodeState.FIELDS:
+            setattr(s, f, self.states[f][i])
+        return s
+
+    def restore(self, n):
+        for f in self.E.DecodeState.FIELDS:
+            src = getattr(self.pristine, f)
+            self.states[f][:n].copy_(src.unsqueeze(0).expand(n, *src.shape))
+
+    def one(self, i, slot):
+        c = self.copies[i % len(self.copies)]
+        self.E.step(self.p, self.state(slot), c["logits"], self.cand_pos, self.cand_count,
+                    [dict(k_cache=c["k_cache"], v_cache=c["v_cache"], k_src=c["k_src"], v_src=c["v_src"],
+                          q_src=c["q_src"], out=c["out"])], ws=self.ws)
+
+    def capture(self, n):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.restore(n)
+                for i in range(n):
+                    self.one(i, i)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    def warm_eager(self, n):
+        """n eager steps; returns (flag of sequence max, R summed over the batch)."""
+        import torch
+
+        self.restore(self.nstate)
+        for i in range(n):
+            self.one(i, i % self.nstate)
+        torch.cuda.synchronize()
+        st0 = self.state(0)
+        status, word = self.E.read_device_error(st0.dev_err)
+        if status != 0:
+            raise RuntimeError(f"device error word {word:#x} during warm-up")
+        return int(st0.flag.max().item()), int(st0.R.sum().item()), st0
+
+    def check(self):
+        status, word = self.E.read_device_error(self.state(0).dev_err)
+        if status != 0:
+            raise RuntimeError(f"device error word {word:#x} during the timed steps")
+
+
+def replay_ms(graphs, dev):
+    """CUDA-event time of one pass over `graphs` (each replayed once, in order)."""
+    import torch
+
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for g in graphs:
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def warm_replay(g, min_ms=100.0):
+    """Untimed replays of g for at least min_ms of wall time: clocks and caches settle before
+    a timed region, whatever its length."""
+    import torch
+
+    t0 = time.perf_counter()
+    while (time.perf_counter() - t0) * 1e3 < min_ms:
+        g.replay()
+        torch.cuda.synchronize()
+
+
 def run_ours(args, rank: int, world: int) -> dict | None:
     import torch
 
@@ -244,80 +395,24 @@ def run_ours(args, rank: int, world: int) -> dict | None:
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = bench_workload(args)
-    p = E.Params(B=w.B, L=w.L, Hq=w.Hq, Hkv=w.Hkv, D=w.D, V=w.V, C_max=w.C_max, k=w.k, n_dec=w.n_dec, tau=w.tau,
-                 logits_dtype=w.logits_dtype)
+    p = params_of(E, w)
     K, Wm = args.steps, args.warmup
     st_h = W.snapshot_state(w)
-    lg_h = W.step_logits(w)
-    lay_h = W.layer_tensors(w, 0)
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    base = {n: bf(lay_h[n]) for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
-    base["logits"] = bf(lg_h) if w.logits_dtype == "bf16" else torch.from_numpy(lg_h).to(dev)
+    base, lg_h, lay_h = host_inputs(w, dev)
     copies = []
     for c in range(NCOPY):
         d = {n: t.clone() for n, t in base.items()}
         d["out"] = torch.zeros(w.B, w.L, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
         copies.append(d)
-    cand_pos = torch.from_numpy(st_h["cand_pos"]).to(dev)
-    cand_count = torch.from_numpy(st_h["cand_count"]).to(dev)
-    ws = E.workspace(E.step_workspace_size(p), dev)
+    del base
 
-    # per-step decode states, restored from a pristine copy at the start of every graph
     G = max(1, min(CHUNK, K))
-    nstate = max(G, Wm, 1)
-    pristine = E.DecodeState.from_arrays(p, device=dev, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
-                                         ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
-    states = {f: getattr(pristine, f).unsqueeze(0).repeat(nstate, *([1] * getattr(pristine, f).dim())).contiguous()
-              for f in E.DecodeState.FIELDS}
-
-    def state_view(i):
-        s = object.__new__(E.DecodeState)
-        for f in E.DecodeState.FIELDS:
-            setattr(s, f, states[f][i])
-        return s
-
-    def restore(n):
-        for f in E.DecodeState.FIELDS:
-            states[f][:n].copy_(getattr(pristine, f).unsqueeze(0).expand(n, *getattr(pristine, f).shape))
-
-    def one_step(i, slot):
-        c = copies[i % NCOPY]
-        E.step(p, state_view(slot), c["logits"], cand_pos, cand_count,
-               [dict(k_cache=c["k_cache"], v_cache=c["v_cache"], k_src=c["k_src"], v_src=c["v_src"],
-                     q_src=c["q_src"], out=c["out"])], ws=ws)
-
-    # warm-up (eager)
-    restore(nstate)
-    for i in range(Wm):
-        one_step(i, i)
-    torch.cuda.synchronize()
-    st0 = state_view(0)
-    status, word = E.read_device_error(st0.dev_err)
-    if status != 0:
-        raise RuntimeError(f"device error word {word:#x} during warm-up")
-    flag = int(st0.flag.max().item())
-    R = int(st0.R.sum().item())
-
-    def capture(n):
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                restore(n)
-                for i in range(n):
-                    one_step(i, i)
-        torch.cuda.current_stream().wait_stream(s)
-        return g
-
-    g_main = capture(G)
+    loop = StepLoop(E, p, w, copies, st_h, dev, max(G, Wm, STEADY_CHUNK, 1))
+    flag, R, st0 = loop.warm_eager(Wm)
+    g_main = loop.capture(G)
     rem = K % G
-    g_rem = capture(rem) if rem else None
-    g_main.replay()  # one untimed replay to settle the graph
-    torch.cuda.synchronize()
+    g_rem = loop.capture(rem) if rem else None
+    warm_replay(g_main)  # untimed: the timed region starts on a settled GPU
 
     barrier(world)
     torch.cuda.synchronize()
@@ -331,22 +426,195 @@ def run_ours(args, rank: int, world: int) -> dict | None:
         t1.record()
         torch.cuda.synchronize()
     ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    status, word = E.read_device_error(state_view(0).dev_err)
-    if status != 0:
-        raise RuntimeError(f"device error word {word:#x} during the timed steps")
+    loop.check()
 
     copy_mb = sum(t.numel() * t.element_size() for t in copies[0].values()) / 1e6
     res = {"ms": ms, "flag": flag, "R": R, "clocks": clk.summary(), "copy_mb": copy_mb}
+    # steady-state rate: the median over repeats of 4 x STEADY_CHUNK graph-replayed steps
+    g_st = loop.capture(STEADY_CHUNK)
+    warm_replay(g_st, 50.0)
+    reps = [4 * STEADY_CHUNK / (replay_ms([g_st] * 4, dev) / 1e3) for _ in range(STEADY_REPEATS)]
+    loop.check()
+    res["steady"] = {"steps_per_s": statistics.median(reps), "repeats": STEADY_REPEATS,
+                     "steps_each": 4 * STEADY_CHUNK, "spread": [min(reps), max(reps)]}
+    del g_main, g_rem, g_st
     if rank == 0:
-        res["kernels"] = time_kernels(E, p, w, copies, st0, dev, min(K, 2000))
+        res["kernels"] = time_kernels(E, p, w, copies, st0, dev, min(K, 2000) if K >= 200 else 2000)
         per_step = sum(lay_h[n].nbytes for n in ("k_src", "v_src", "q_src")) + lg_h.nbytes
         n_e2e = max(10, min(K, 2000, int(20e9 // per_step)))  # at most ~20 GB of host->device traffic
         res["e2e"] = run_e2e(E, p, w, lay_h, lg_h, st_h, dev, n_e2e)
-    del g_main, g_rem
+        del copies, loop
+        torch.cuda.empty_cache()
+        if not args.no_configs:
+            res["configs"] = run_configs(E, dev, args)
     return res
 
 
-def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
+def config_entry(E, w, dev, n_steps, inputs: str, seed: int) -> dict:
+    """steps/s and per-kernel times of one workload's single step (see run_configs)."""
+    import torch
+
+    p = params_of(E, w)
+    st_h = W.snapshot_state(w)
+    if inputs == "host":
+        base, _, _ = host_inputs(w, dev)
+    else:
+        lg_h = W.step_logits(w)
+        lg = (torch.from_numpy(lg_h.view(np.int16)).to(dev).view(torch.bfloat16) if w.logits_dtype == "bf16"
+              else torch.from_numpy(lg_h).to(dev))
+        base = device_inputs(w, dev, seed, logits=lg)
+    copies, per = make_copies(base, w, dev)
+    del base
+    G = max(1, min(CHUNK, n_steps))
+    loop = StepLoop(E, p, w, copies, st_h, dev, G)
+    flag, R, st0 = loop.warm_eager(3)
+    g = loop.capture(G)
+    warm_replay(g, 50.0)
+    reps = max(1, n_steps // G)
+    ms = replay_ms([g] * reps, dev)
+    loop.check()
+    kern = time_kernels(E, p, w, copies, st0, dev, min(2000, max(50, n_steps)), lm_head=False)
+    del g, loop, copies
+    torch.cuda.empty_cache()
+    return summarise_config(w, reps * G / (ms / 1e3), flag, R, kern, per, inputs)
+
+
+def summarise_config(w, steps_per_s, flag, R, kern, per_copy_bytes, inputs) -> dict:
+    """One `configs` entry: the step rate and each kernel against its binding roofline."""
+    pk = peaks()
+    alg = algorithmic(w, R)
+    ent_gbs = alg["entropy_decode_bytes"] / (kern["entropy_decode_us"] * 1e3)
+    att_gbs = alg["partial_attention_bytes"] / (kern["partial_attention_us"] * 1e3)
+    att_tfs = alg["partial_attention_flops"] / (kern["partial_attention_us"] * 1e6)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    intensity = alg["partial_attention_flops"] / alg["partial_attention_bytes"]
+    att_bound = "tensor" if intensity > ridge else "hbm"
+    return {
+        "workload": workload_desc(w),
+        "step": f"{'full' if flag else 'partial'} (R={R} over the batch)",
+        "steps_per_s": steps_per_s,
+        "us_per_step": 1e6 / steps_per_s,
+        "inputs": inputs,
+        "l2": f"inputs rotate over copies of {per_copy_bytes / 1e6:.1f} MB, at least 256 MB per rotation",
+        "entropy_decode": {"us": kern["entropy_decode_us"], "GB/s": ent_gbs, "frac_hbm": ent_gbs / pk["hbm_gbs"]},
+        "partial_attention": {"us": kern["partial_attention_us"], "GB/s": att_gbs, "TFLOP/s": att_tfs,
+                              "flop_per_byte": intensity, "bound": att_bound,
+                              "frac_hbm": att_gbs / pk["hbm_gbs"], "frac_bf16": att_tfs / pk["bf16_tflops"],
+                              "frac_bound": (att_tfs / pk["bf16_tflops"]) if att_bound == "tensor"
+                              else att_gbs / pk["hbm_gbs"]},
+        "kv_scatter": {"us": kern["kv_scatter_us"]},
+        "decision_us": kern["entropy_decode_us"],
+    }
+
+
+def trace_logits_device(w, step, gen, dev):
+    """Candidate logits of one step of the decode trace, drawn on the device with the trace
+    recipe of the workloads module (high-entropy steps N(0, 0.5^2); low ones N(0, 1) with one
+    peak per row of height 17.25 - 0.25 (c - 1 - i)), bf16."""
+    import torch
+
+    B, C, V = w.B, w.C_max, w.V
+    out = torch.empty(B, C, V, dtype=torch.float32, device=dev)
+    c = w.block - step % w.block
+    height = (17.25 - 0.25 * (c - 1 - torch.arange(C, device=dev))).float()
+    for b in range(B):
+        if W.trace_is_high(w, step, b):
+            out[b] = torch.randn(C, V, generator=gen, device=dev) * 0.5
+        else:
+            out[b] = torch.randn(C, V, generator=gen, device=dev)
+            peak = torch.randint(0, V, (C,), generator=gen, device=dev)
+            out[b, torch.arange(C, device=dev), peak] = height
+    return out.to(torch.bfloat16)
+
+
+def run_trace(E, dev, n_steps) -> dict:
+    """A timed stretch of the 256-step decode trace over the 32-layer LLaDA-shaped attention
+    stack (B 4, 32 x 128, L 4096): the first n_steps steps of the trajectory, each one ec_step
+    over all 32 layers, replayed from one CUDA graph (state restored inside). The same stretch
+    with no layers (stages (a)-(c) alone) gives the decision share of the step time."""
+    import torch
+
+    w = W.workload(4)
+    p = params_of(E, w)
+    st_h = W.snapshot_state(w)
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    layers = []
+    for l in range(w.n_layers):
+        d = device_inputs(w, dev, 1000 + l)
+        d["out"] = torch.zeros(w.B, w.L, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+        layers.append(d)
+    logits = [trace_logits_device(w, t, gen, dev) for t in range(n_steps)]
+    ws = E.workspace(E.step_workspace_size(p), dev)
+    init = dict(tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"], ring_head=st_h["ring_head"],
+                ring_count=st_h["ring_count"])
+    pristine = E.DecodeState.from_arrays(p, device=dev, **init)
+    st = pristine.clone()
+    # discovery pass: each step's candidates are the still-masked positions of its block
+    cands, n_full = [], 0
+    mask = st_h["mask"].copy()
+    for t in range(n_steps):
+        cp, cc = W.trace_candidates(w, mask, t)
+        cands.append((torch.from_numpy(cp).to(dev), torch.from_numpy(cc).to(dev)))
+        E.step(p, st, logits[t].view(w.B * w.C_max, w.V), cands[t][0], cands[t][1], layers, ws=ws)
+        mask = st.mask.cpu().numpy()
+        n_full += int(st.flag.sum().item())
+    status, word = E.read_device_error(st.dev_err)
+    if status != 0:
+        raise RuntimeError(f"device error word {word:#x} in the trace")
+
+    def capture(with_layers):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for f in E.DecodeState.FIELDS:
+                    getattr(st, f).copy_(getattr(pristine, f))
+                for t in range(n_steps):
+                    E.step(p, st, logits[t].view(w.B * w.C_max, w.V), cands[t][0], cands[t][1],
+                           layers if with_layers else [], ws=ws)
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    g_all, g_dec = capture(True), capture(False)
+    g_all.replay()
+    g_dec.replay()
+    torch.cuda.synchronize()
+    t_all = statistics.median(replay_ms([g_all], dev) for _ in range(3))
+    t_dec = statistics.median(replay_ms([g_dec] * 10, dev) / 10 for _ in range(3))
+    status, word = E.read_device_error(st.dev_err)
+    if status != 0:
+        raise RuntimeError(f"device error word {word:#x} in the timed trace")
+    del g_all, g_dec, layers, logits
+    torch.cuda.empty_cache()
+    return {
+        "workload": (f"{w.name}: B{w.B}, {w.Hq}x{w.D} MHA, {w.n_layers} layers, L={w.L} ({w.prompt}+{w.gen}, block "
+                     f"{w.block}), k={w.k}, V={w.V} bf16 logits, tau={w.tau}; steps 0..{n_steps - 1} of {w.steps}"),
+        "steps": n_steps,
+        "full_fraction": n_full / (n_steps * w.B),
+        "steps_per_s": n_steps / (t_all / 1e3),
+        "ms_per_step": t_all / n_steps,
+        "decision_us_per_step": t_dec * 1e3 / n_steps,
+        "decision_share": t_dec / t_all,
+        "decision": "stages (a)-(c1): the decode kernel and the select kernel, timed as the same steps with no layers",
+        "inputs": "K/V/Q drawn on the device per layer; logits drawn on the device with the trace recipe",
+    }
+
+
+def run_configs(E, dev, args) -> dict:
+    """Every synthetic workload besides the headline: workload 1 (tiny, fp32 logits), the
+    headline layer with tau below every entropy (a full step, R = L), workload 3 (the Dream-7B
+    GQA batch), workload 5 (the 32K-row cache) and a stretch of the workload-4 trace."""
+    out = {}
+    out["tiny"] = config_entry(E, W.workload(1), dev, 2000, "host", 1)
+    out["llada_layer_full"] = config_entry(E, W.workload(2).scaled(tau=-1.0), dev, 500, "host", 2)
+    out["dream_gqa"] = config_entry(E, W.workload(3), dev, 50, "device", 3)
+    out["long_context"] = config_entry(E, W.workload(5), dev, 500, "device", 5)
+    out["llada_trace"] = run_trace(E, dev, args.trace_steps)
+    return out
+
+
+def time_kernels(E, p, w, copies, st0, dev, n, lm_head=True) -> dict:
     """Average duration of each stage's kernel, timed alone through its own entry point over
     the rotating input copies (CUDA events on the launching stream, graph-replayed)."""
     import torch
@@ -368,16 +636,18 @@ def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
             c["qfull"][b, :r] = c["q_src"][b, idx[b, :r].long()]
     torch.cuda.synchronize()
 
+    nc = len(copies)
+
     def stage_entropy(i):
-        c = copies[i % NCOPY]
+        c = copies[i % nc]
         E.entropy_decode(c["logits"].view(rows, w.V), ws=ent_ws, out=(ids, ent, conf))
 
     def stage_attention(i):
-        c = copies[i % NCOPY]
+        c = copies[i % nc]
         E.partial_attention(p, c["qfull"], c["k_cache"], c["v_cache"], R, c["out"], ws=att_ws)
 
     def stage_scatter(i):
-        c = copies[i % NCOPY]
+        c = copies[i % nc]
         E.kv_scatter(p, c["k_cache"], c["v_cache"], c["k_src"], c["v_src"], idx, R, src_by_position=True)
 
     def timed(fn, n):
@@ -406,7 +676,7 @@ def time_kernels(E, p, w, copies, st0, dev, n) -> dict:
 
     # stage (a) from the hidden states: the output projection fused with the decode, on a
     # random bf16 weight of the model's shape (V x d_model, about 1 GB: no L2 reuse)
-    if w.d_model > 0:
+    if lm_head and w.d_model > 0:
         g = torch.Generator(device=dev).manual_seed(w.seed)
         hid = torch.randn(rows, w.d_model, device=dev, generator=g).to(torch.bfloat16)
         wt = (torch.randn(w.V, w.d_model, device=dev, generator=g) / w.d_model ** 0.5).to(torch.bfloat16)
@@ -602,7 +872,8 @@ def emit_ours(args, res, rank, world):
         "data": "synthetic",
         "config": {"workload": workload_desc(w), "step": f"{'full' if res['flag'] else 'partial'} (R={res['R']} over the batch)",
                    "l2": f"inputs rotate over {NCOPY} copies ({NCOPY} x {res['copy_mb']:.0f} MB; L2 is 129 MB)",
-                   "timing": f"CUDA graphs of {min(CHUNK, K)} steps, state restore inside"},
+                   "timing": (f"CUDA graphs of {min(CHUNK, K)} steps, state restore inside, after at least 100 ms "
+                              f"of untimed replays")},
         "roofline": roof,
         "kernels": {
             "entropy_decode": {"us": kern["entropy_decode_us"], "GB/s": ent_gbs, "frac_hbm": ent_gbs / pk["hbm_gbs"]},
@@ -614,6 +885,22 @@ def emit_ours(args, res, rank, world):
         "gpu_launches": 4 * K,
         "clocks": res["clocks"],
     }
+    if "steady" in res:
+        line["steady"] = res["steady"]
+    targets = {"entropy_decode_hbm": {"kernel": "entropy_decode", "workload": w.name, "frac": ent_gbs / pk["hbm_gbs"],
+                                      "goal": 0.70, "of": "measured HBM copy bandwidth"}}
+    cfg = res.get("configs") or {}
+    if "llada_layer_full" in cfg:
+        fa = cfg["llada_layer_full"]["partial_attention"]
+        targets["attention_bf16"] = {"kernel": "partial_attention", "workload": "llada_layer, full step (R = L)",
+                                     "frac": fa["frac_bf16"], "goal": 0.50, "of": "measured bf16 dense (cuBLAS burst)"}
+    if "dream_gqa" in cfg:
+        targets["entropy_decode_hbm_dream"] = {"kernel": "entropy_decode", "workload": "dream_gqa (78 MB)",
+                                               "frac": cfg["dream_gqa"]["entropy_decode"]["frac_hbm"],
+                                               "of": "measured HBM copy bandwidth"}
+    line["targets"] = targets
+    if cfg:
+        line["configs"] = cfg
     if "lm_head_entropy_us" in kern:  # not part of the timed step, which starts from logits
         lm_gbs = kern["lm_head_bytes"] / (kern["lm_head_entropy_us"] * 1e3)
         line["kernels"]["lm_head_entropy"] = {"us": kern["lm_head_entropy_us"], "GB/s": lm_gbs,
@@ -628,8 +915,9 @@ def emit_ours(args, res, rank, world):
 
 
 class OracleStep:
-    """Times the float64 oracle on a bounded sample of the workload's step and scales the
-    sampled stages to a whole step."""
+    """The float64 oracle's whole step on the headline workload: decode and entropy of every
+    candidate row, commit, gate, history, recompute set, K/V refresh and attention of every
+    recompute row over all heads (oracle.step). Nothing is sampled."""
 
     def __init__(self):
         import oracle as O
@@ -640,41 +928,14 @@ class OracleStep:
         self.st = W.snapshot_state(w)
         self.x = O.widen(W.step_logits(w)[0], w.logits_dtype)
         lay = W.layer_tensors(w, 0)
-        self.kc = O.widen(lay["k_cache"][0], "bf16")
-        self.vc = O.widen(lay["v_cache"][0], "bf16")
-        self.ks = O.widen(lay["k_src"][0], "bf16")
-        self.vs = O.widen(lay["v_src"][0], "bf16")
-        self.qs = O.widen(lay["q_src"][0], "bf16")
+        self.layer = {n: O.widen(lay[n][0], "bf16") for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
 
-    def run(self, n_rows: int, n_attn: int, rng) -> float:
-        """One sampled step; returns the time scaled to a whole step (seconds)."""
-        O, w, st = self.O, self.w, self.st
-        C = int(st["cand_count"][0])
-        t0 = time.perf_counter()
-        rows = rng.choice(C, size=min(n_rows, C), replace=False)
-        for i in rows:
-            O.entropy_decode_row(self.x[i])
-        t1 = time.perf_counter()
-        # stages (b)(c) in full, on the full candidate list (entropies from a cheap stand-in)
-        conf = -np.arange(C, dtype=np.float64)
-        ent = np.full(C, 0.5)
-        dec = O.select_decoded(st["cand_pos"][0], C, conf, w.n_dec)
-        mask = st["mask"][0].copy()
-        for i in dec:
-            mask[st["cand_pos"][0][i]] = 0
-        E_ = O.max_entropy(ent, dec)
-        full = O.recompute_flag(E_, w.tau)
-        ring, head, cnt = O.history_push(st["ring"][0], int(st["ring_head"][0]), int(st["ring_count"][0]),
-                                         [int(st["cand_pos"][0][i]) for i in dec])
-        idx = O.recompute_set(mask, O.history_last(ring, head, cnt), full)
-        kc = O.kv_scatter(self.kc, idx, self.ks[idx])
-        vc = O.kv_scatter(self.vc, idx, self.vs[idx])
-        t2 = time.perf_counter()
-        R = len(idx)
-        sel = rng.choice(R, size=min(n_attn, R), replace=False)
-        O.attention(self.qs[idx[sel]], kc, vc, 1.0 / math.sqrt(w.D))
-        t3 = time.perf_counter()
-        return (t1 - t0) * C / len(rows) + (t2 - t1) + (t3 - t2) * R / len(sel)
+    def run(self) -> dict:
+        st = self.st
+        return self.O.step(logits=self.x, cand_pos=st["cand_pos"][0], cand_count=int(st["cand_count"][0]),
+                           tokens=st["tokens"][0], mask=st["mask"][0], ring=st["ring"][0],
+                           ring_head=int(st["ring_head"][0]), ring_count=int(st["ring_count"][0]),
+                           n_dec=self.w.n_dec, tau=self.w.tau, layers=[self.layer])
 
 
 def cpu_cores() -> int:
@@ -684,47 +945,59 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def time_oracle(os_: OracleStep, n: int | None = None, budget_s: float | None = None) -> dict:
+    """Runs whole oracle steps (n of them, or as many as fit in budget_s) and returns the rate,
+    the wall time and the threads actually used (process CPU time over wall time: NumPy's BLAS
+    may run the attention products on several threads)."""
+    c0, t0 = time.process_time(), time.perf_counter()
+    k = 0
+    while (n is not None and k < n) or (budget_s is not None and (k < 1 or time.perf_counter() - t0 < budget_s)):
+        os_.run()
+        k += 1
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return {"steps": k, "wall_s": wall, "rate": k / wall, "threads": max(1, round(cpu / wall))}
+
+
 def cpu_baseline(budget_s: float = 15.0) -> dict:
     os_ = OracleStep()
-    rng = np.random.default_rng(0)
-    total, n, t_start = 0.0, 0, time.perf_counter()
-    while n < 1 or time.perf_counter() - t_start < budget_s:
-        total += os_.run(8, 8, rng)
-        n += 1
-    return {"value": n / total, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": (f"{n} steps of the float64 oracle; each runs 8 of 32 candidate rows of the entropy stage and "
-                       f"8 of the R recompute rows of attention (all heads), stages (b)(c) in full; stage times "
-                       f"scaled to a whole step"), "wall_s": time.perf_counter() - t_start}
+    os_.run()  # warm
+    r = time_oracle(os_, budget_s=budget_s)
+    return {"value": r["rate"], "unit": "steps/s", "cores": r["threads"], "cores_available": cpu_cores(),
+            "kind": "oracle",
+            "sample": (f"full step: {r['steps']} whole float64 oracle steps of the headline workload (all "
+                       f"{int(os_.st['cand_count'][0])} candidate rows, every recompute row over all heads), "
+                       f"no sampling; cores = process CPU time / wall time"), "wall_s": r["wall_s"]}
 
 
 def run_reference(args) -> None:
     os_ = OracleStep()
-    rng = np.random.default_rng(1)
     K, Wm = args.steps, args.warmup
-    per_step_budget = min(1.0, 120.0 / max(1, K + Wm))
-    # size the sample so a step fits its budget: time one entropy row and one attention row
     t0 = time.perf_counter()
-    os_.run(1, 1, rng)
-    t_probe = time.perf_counter() - t0
-    n = max(1, int(per_step_budget / max(t_probe, 1e-4)))
-    n = min(n, 32)
-    for _ in range(Wm):
-        os_.run(n, n, rng)
-    total = 0.0
-    wall0 = time.perf_counter()
-    for _ in range(K):
-        total += os_.run(n, n, rng)
-    wall = time.perf_counter() - wall0
-    value = K / total
+    os_.run()
+    t_step = time.perf_counter() - t0
+    budget = 150.0  # the whole --steps K --warmup W run stays within a few minutes
+    if (K + Wm) * t_step <= budget:
+        for _ in range(Wm):
+            os_.run()
+        r = time_oracle(os_, n=K)
+        sample = f"full step: each of {K} steps is a whole float64 oracle step, no sampling"
+    else:  # K too large to run in full: time as many whole steps as the budget allows
+        for _ in range(min(Wm, 3)):
+            os_.run()
+        r = time_oracle(os_, budget_s=budget)
+        sample = (f"full steps: {r['steps']} whole float64 oracle steps timed within a {budget:.0f} s budget (the "
+                  f"{K} requested steps would take {K * t_step:.0f} s); value = their rate")
+    value = r["rate"]
     w = W.workload(WORKLOAD)
-    cb = {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-          "sample": (f"each of {K} steps runs {n} of 32 candidate rows of the entropy stage and {n} of the R "
-                     f"recompute rows of attention (all heads) in float64, stages (b)(c) in full; stage times "
-                     f"scaled to a whole step"), "wall_s": wall}
+    cb = {"value": value, "unit": "steps/s", "cores": r["threads"], "cores_available": cpu_cores(), "kind": "oracle",
+          "sample": sample + "; cores = process CPU time / wall time", "wall_s": r["wall_s"]}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": 1, "steps": K,
             "warmup": Wm, "ms_per_step": 1e3 / value, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w)}, "cpu_baseline": cb,
+            "config": {"workload": workload_desc(w), "step": "partial (R=95 over the batch)",
+                       "l2": "host memory (CPU oracle)", "timing": "wall clock over whole oracle steps"},
+            "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -740,6 +1013,8 @@ def main():
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 5],
                     help="workload to time (default 2, the LLaDA-8B layer step)")
     ap.add_argument("--tau", type=float, default=None, help="override tau (e.g. -1 forces a full step)")
+    ap.add_argument("--no-configs", action="store_true", help="time only the headline workload")
+    ap.add_argument("--trace-steps", type=int, default=64, help="steps of the decode trace timed under configs")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="run this many eager steps and exit (a short program for ncu)")
     args = ap.parse_args()

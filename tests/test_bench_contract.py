@@ -120,3 +120,24 @@ def test_reference_arm_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+
+
+def test_config_entry_against_its_binding_roofline():
+    # A `configs` entry from a synthetic measurement: the decode against HBM, the attention
+    # against the roofline its arithmetic intensity selects (tensor above the ridge, else HBM).
+    import workloads as W
+
+    pk = bench.peaks()
+    kern = {"entropy_decode_us": 8.0, "partial_attention_us": 20.0, "kv_scatter_us": 3.0}
+    w = W.workload(2)
+    e = bench.summarise_config(w, 20000.0, 1, 1024, kern, 50e6, "host")  # a full step, R = L
+    alg = bench.algorithmic(w, 1024)
+    assert e["us_per_step"] == pytest.approx(50.0)
+    assert e["entropy_decode"]["GB/s"] == pytest.approx(alg["entropy_decode_bytes"] / 8e-6 / 1e9)
+    att = e["partial_attention"]
+    assert att["bound"] == "tensor"  # 512 flops per byte
+    assert att["TFLOP/s"] == pytest.approx(alg["partial_attention_flops"] / 20e-6 / 1e12)
+    assert att["frac_bound"] == pytest.approx(att["TFLOP/s"] / pk["bf16_tflops"])
+    e = bench.summarise_config(w, 40000.0, 0, 95, kern, 50e6, "host")  # partial: 87 flops per byte
+    assert e["partial_attention"]["bound"] == "hbm"
+    assert e["partial_attention"]["frac_bound"] == pytest.approx(e["partial_attention"]["frac_hbm"])

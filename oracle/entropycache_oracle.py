@@ -48,6 +48,8 @@ __all__ = [
     "history_push",
     "history_last",
     "recompute_set",
+    "block_candidates",
+    "sliding_window_candidates",
     "kv_scatter",
     "attention",
     "step",
@@ -188,18 +190,45 @@ def history_last(ring: np.ndarray, head: int, count: int) -> list[int]:
     return [int(ring[(head - 1 - t) % k]) for t in range(n)]
 
 
-def recompute_set(mask: np.ndarray, recent: list[int], full: bool) -> np.ndarray:
+def recompute_set(mask: np.ndarray, recent: list[int], full: bool,
+                  scope: tuple[int, int] | None = None) -> np.ndarray:
     """Recompute set of one sequence, ascending ([zh] §2.2 partial forward; [pt] §2).
 
     Full step: every position. Partial step: still-masked positions union the k most recently
     decoded positions.
+
+    With a scope (lo, hi) — block-by-block decoding, where the gate is a recompute signal for
+    the block being decoded ([zh] §5, sub-block recompute in block diffusion) — every position
+    considered is restricted to [lo, hi): a full step recomputes the block, a partial one the
+    block's masked positions and the recent positions that lie in the block.
     """
     L = mask.shape[0]
+    lo, hi = (0, L) if scope is None else (int(scope[0]), int(scope[1]))
     if full:
-        return np.arange(L, dtype=np.int64)
-    chosen = set(int(p) for p in np.flatnonzero(mask))
-    chosen.update(int(p) for p in recent)
+        return np.arange(lo, hi, dtype=np.int64)
+    chosen = set(int(p) for p in np.flatnonzero(mask) if lo <= p < hi)
+    chosen.update(int(p) for p in recent if lo <= p < hi)
     return np.array(sorted(chosen), dtype=np.int64)
+
+
+# --------------------------------------------------------------------------------------
+# decoding schedules the gate carries over to  —  [pt] §5 "Generalidade", [zh] §5
+
+
+def block_candidates(mask: np.ndarray, start: int, width: int) -> list[int]:
+    """Candidates of a block-decoding step: the masked positions of the block
+    [start, start + width), ascending (clipped to the sequence)."""
+    L = mask.shape[0]
+    return [p for p in range(int(start), min(L, int(start) + int(width))) if mask[p]]
+
+
+def sliding_window_candidates(mask: np.ndarray, start: int, width: int) -> list[int]:
+    """Candidates of a sliding-window decoding step: the window begins at the first masked
+    position at or after `start` and spans `width` positions; its masked positions,
+    ascending. The window slides forward as its earliest position gets decoded."""
+    L = mask.shape[0]
+    f = next((p for p in range(int(start), L) if mask[p]), L)
+    return [p for p in range(f, min(L, f + int(width))) if mask[p]]
 
 
 def kv_scatter(cache: np.ndarray, idx: np.ndarray, fresh_rows: np.ndarray) -> np.ndarray:
@@ -259,6 +288,7 @@ def step(
     scale: float | None = None,
     attention_rows: np.ndarray | None = None,
     decoded_rows: list[int] | None = None,
+    scope: tuple[int, int] | None = None,
 ) -> dict:
     """One denoising step of one sequence.
 
@@ -270,6 +300,9 @@ def step(
     decoded_rows optionally fixes the committed candidate rows instead of ranking them: a
     checker that finds two candidates' confidences tied within rounding adopts the device's
     choice among them this way, then checks everything that follows from it.
+    scope (lo, hi), for block-by-block decoding: the recompute set is restricted to the block
+    (recompute_set) and the recomputed rows attend to the keys [0, hi) only: the block and the
+    blocks before it, none after it (block-causal attention).
     Returns decode results, the gate, the new state, idx and per-layer outputs.
     """
     C = int(cand_count)
@@ -288,7 +321,8 @@ def step(
     full = recompute_flag(E, tau)
     dec_positions = [int(cand_pos[i]) for i in rows]
     ring2, head2, count2 = history_push(ring, ring_head, ring_count, dec_positions)
-    idx = recompute_set(mask, history_last(ring2, head2, count2), full)
+    idx = recompute_set(mask, history_last(ring2, head2, count2), full, scope)
+    hi = mask.shape[0] if scope is None else int(scope[1])
     out_layers = []
     for lay in layers or []:
         kc = kv_scatter(lay["k_cache"], idx, lay["k_src"][idx])
@@ -296,7 +330,7 @@ def step(
         D = kc.shape[-1]
         sc = (1.0 / math.sqrt(D)) if scale is None else scale
         sel = idx if attention_rows is None else idx[attention_rows]
-        o = attention(lay["q_src"][sel], kc, vc, sc)
+        o = attention(lay["q_src"][sel], kc[:hi], vc[:hi], sc)
         out_layers.append({"k_cache": kc, "v_cache": vc, "out": o})
     return {
         "ids": ids,

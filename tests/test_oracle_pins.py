@@ -391,3 +391,130 @@ def test_confidence_threshold_commit_by_hand():
     # NaN confidence never passes and ranks last
     lc2 = np.array([math.nan, math.log(0.8), math.log(0.2)])
     assert O.select_decoded(pos[:3], 3, lc2, 3, conf_threshold=0.5) == [1]
+
+
+# --------------------------------------------------------------------------------------
+# decoding schedules and the block-scoped gate ([pt] §5 "Generalidade", [zh] §5)
+
+
+def test_scoped_recompute_set_exhaustive_small():
+    # membership scan over every mask of L <= 8 and every scope [lo, hi)
+    rng = np.random.default_rng(14)
+    for L in range(1, 9):
+        for bits in range(1 << L):
+            mask = np.array([(bits >> p) & 1 for p in range(L)], dtype=np.uint8)
+            recent = [int(v) for v in rng.choice(L, size=int(rng.integers(0, L + 1)), replace=False)]
+            for lo in range(L):
+                for hi in range(lo + 1, L + 1):
+                    got = O.recompute_set(mask, recent, full=False, scope=(lo, hi)).tolist()
+                    want = []
+                    for p in range(L):
+                        inside = lo <= p and p < hi
+                        if inside and (mask[p] == 1 or p in recent):
+                            want.append(p)
+                    assert got == want, (L, bits, lo, hi)
+                    assert O.recompute_set(mask, recent, full=True, scope=(lo, hi)).tolist() == list(range(lo, hi))
+            # the whole sequence as the scope is the unscoped set
+            assert (O.recompute_set(mask, recent, False, (0, L)).tolist()
+                    == O.recompute_set(mask, recent, False).tolist())
+
+
+def test_schedule_candidates_by_hand():
+    mask = np.array([0, 0, 1, 0, 1, 1, 0, 1, 1, 0, 0, 1], dtype=np.uint8)  # masked: 2 4 5 7 8 11
+    assert O.block_candidates(mask, 0, 4) == [2]
+    assert O.block_candidates(mask, 4, 4) == [4, 5, 7]
+    assert O.block_candidates(mask, 8, 4) == [8, 11]
+    assert O.block_candidates(mask, 10, 8) == [11]  # clipped at L = 12
+    assert O.block_candidates(mask, 0, 2) == []
+    # sliding: the window opens at the first masked position at or after start
+    assert O.sliding_window_candidates(mask, 0, 4) == [2, 4, 5]  # window 2..5
+    assert O.sliding_window_candidates(mask, 3, 4) == [4, 5, 7]  # window 4..7
+    assert O.sliding_window_candidates(mask, 6, 2) == [7, 8]  # window 7..8
+    assert O.sliding_window_candidates(mask, 9, 5) == [11]  # window 11..15, clipped
+    assert O.sliding_window_candidates(np.zeros(5, np.uint8), 0, 3) == []  # nothing masked
+
+
+def test_schedule_candidates_invariants():
+    rng = np.random.default_rng(15)
+    for _ in range(400):
+        L = int(rng.integers(1, 40))
+        mask = (rng.random(L) < rng.random()).astype(np.uint8)
+        W = int(rng.integers(1, 12))
+        start = int(rng.integers(0, L))
+        # blocks of width W tile the sequence: their candidates partition the masked positions
+        tiles = [p for b0 in range(0, L, W) for p in O.block_candidates(mask, b0, W)]
+        assert tiles == [int(p) for p in np.flatnonzero(mask)]
+        got = O.sliding_window_candidates(mask, start, W)
+        later = [int(p) for p in np.flatnonzero(mask) if p >= start]
+        if not later:
+            assert got == []
+            continue
+        assert got[0] == later[0]  # the window opens at the first masked position at or after start
+        assert got == [p for p in later if p < later[0] + W]  # and takes every masked one in W
+
+
+def _brute_scoped(logits, cand_pos, count, mask, decoded_history, tau, k, lo, hi):
+    """List-based restatement of one block-scoped step with n_dec = 1: commit the most
+    confident candidate, gate on its entropy; full: the block; partial: the block's masked
+    positions and the recent positions inside the block."""
+    best = None
+    for i in range(count):
+        x = [float(t) for t in logits[i]]
+        m = max(x)
+        z = sum(math.exp(t - m) for t in x)
+        ps = [math.exp(t - m) / z for t in x]
+        key = (-math.log(ps[x.index(m)]), int(cand_pos[i]))
+        h = -sum(p * math.log(p) for p in ps if p > 0)
+        if best is None or key < best[0]:
+            best = (key, h)
+    mask = list(mask)
+    hist = list(decoded_history)
+    E = 0.0
+    if best is not None:
+        mask[best[0][1]] = 0
+        hist.append(best[0][1])
+        E = best[1]
+    recent = set(hist[-k:])
+    if E > tau:
+        return list(range(lo, hi)), E
+    return [p for p in range(lo, hi) if mask[p] or p in recent], E
+
+
+def test_scoped_step_brute_force_and_block_causal_attention():
+    rng = np.random.default_rng(32)
+    for trial in range(200):
+        L = int(rng.integers(4, 17))
+        lo = int(rng.integers(0, L - 1))
+        hi = int(rng.integers(lo + 1, L + 1))
+        k = int(rng.integers(1, L + 1))
+        mask = np.zeros(L, np.uint8)
+        mask[lo:] = (rng.random(L - lo) < 0.6)  # earlier blocks decoded
+        cand = [p for p in range(lo, hi) if mask[p]]
+        if not cand:
+            mask[lo] = 1
+            cand = [lo]
+        logits = rng.standard_normal((len(cand), 6)) * rng.choice([0.1, 3.0])
+        decoded = [p for p in range(L) if not mask[p]]
+        rng.shuffle(decoded)
+        ring, head, cnt = O.history_push(np.zeros(k, np.int64), 0, 0, decoded)
+        tau = float(rng.choice([0.2, 1.0, 3.0]))
+        got = O.step(logits=logits, cand_pos=np.array(cand), cand_count=len(cand), tokens=np.zeros(L, np.int64),
+                     mask=mask, ring=ring, ring_head=head, ring_count=cnt, n_dec=1, tau=tau, scope=(lo, hi))
+        idx, E = _brute_scoped(logits, cand, len(cand), mask, decoded, tau, k, lo, hi)
+        assert got["idx"].tolist() == idx and abs(got["E"] - E) < 1e-12
+    # attention of a block-scoped full step is dense attention over the keys [0, hi)
+    L, lo, hi, Hq, Hkv, D = 16, 8, 12, 4, 2, 8
+    mask = np.zeros(L, np.uint8)
+    mask[lo:] = 1
+    lay = {n: rng.standard_normal((L, Hkv if n != "q_src" else Hq, D))
+           for n in ("k_cache", "v_cache", "k_src", "v_src", "q_src")}
+    got = O.step(logits=rng.standard_normal((4, 50)) * 0.1, cand_pos=np.arange(lo, hi), cand_count=4,
+                 tokens=np.zeros(L, np.int64), mask=mask, ring=np.zeros(4, np.int64), ring_head=0, ring_count=0,
+                 n_dec=1, tau=1.0, layers=[lay], scope=(lo, hi))
+    assert got["flag"] and got["idx"].tolist() == list(range(lo, hi))
+    kc = lay["k_cache"].copy()
+    vc = lay["v_cache"].copy()
+    kc[lo:hi] = lay["k_src"][lo:hi]
+    vc[lo:hi] = lay["v_src"][lo:hi]
+    want = _sdpa(lay["q_src"][lo:hi], kc[:hi], vc[:hi], 1.0 / math.sqrt(D))
+    np.testing.assert_allclose(got["layers"][0]["out"], want, rtol=1e-12, atol=1e-12)

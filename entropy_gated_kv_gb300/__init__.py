@@ -32,6 +32,7 @@ __all__ = [
     "entropy_decode_workspace_size",
     "entropy_decode_noalloc",
     "select_recompute",
+    "candidates",
     "kv_scatter",
     "partial_attention",
     "partial_attention_workspace_size",
@@ -83,10 +84,13 @@ class Params:
     tau: float = 1.0
     logits_dtype: object = "bf16"
     conf_threshold: float = 0.0  # > 0: commit only candidates at least this confident (at least one)
+    scope_lo: int = 0  # the gate's scope [scope_lo, scope_hi) for block-by-block decoding;
+    scope_hi: int = 0  # both 0: the whole sequence
 
     def c(self) -> C.EcParams:
         return C.EcParams(self.B, self.L, self.Hq, self.Hkv, self.D, self.V, self.C_max, self.k, self.n_dec,
-                          float(self.tau), _dtype_code(self.logits_dtype), float(self.conf_threshold))
+                          float(self.tau), _dtype_code(self.logits_dtype), float(self.conf_threshold),
+                          int(self.scope_lo), int(self.scope_hi))
 
 
 class DecodeState:
@@ -207,6 +211,24 @@ def select_recompute(p: Params, state: DecodeState, cand_pos, cand_count, ids, e
     st = lib().ec_select_recompute(ctypes.byref(pc), ctypes.byref(sc), _vp(cand_pos), _vp(cand_count), _vp(ids),
                                    _vp(entropy), _vp(log_conf), _stream(stream))
     C.check(st, "ec_select_recompute")
+
+
+def candidates(p: Params, state: DecodeState, mode: str, start: int, width: int, cand_pos=None, cand_count=None,
+               stream=None):
+    """Candidates of a block-wise ("block") or sliding-window ("sliding") decoding step: the
+    masked positions of the window, built on the device from state.mask. Returns
+    (cand_pos int32 [B, C_max], cand_count int32 [B])."""
+    code = {"block": C.EC_CAND_BLOCK, "sliding": C.EC_CAND_SLIDING}[mode]
+    dev = state.mask.device
+    if cand_pos is None:
+        cand_pos = torch.empty(p.B, p.C_max, dtype=torch.int32, device=dev)
+    if cand_count is None:
+        cand_count = torch.empty(p.B, dtype=torch.int32, device=dev)
+    pc, sc = p.c(), state.c()
+    st = lib().ec_candidates(ctypes.byref(pc), ctypes.byref(sc), code, int(start), int(width), _vp(cand_pos),
+                             _vp(cand_count), _stream(stream))
+    C.check(st, "ec_candidates")
+    return cand_pos, cand_count
 
 
 def kv_scatter(p: Params, k_cache, v_cache, k_new, v_new, idx, R, src_by_position: bool = False,

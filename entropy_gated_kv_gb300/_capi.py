@@ -24,6 +24,9 @@ EC_DEVERR_TIMEOUT = 0x8
 EC_F32 = 0
 EC_BF16 = 1
 
+EC_CAND_BLOCK = 0
+EC_CAND_SLIDING = 1
+
 EC_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _p = ctypes.c_void_p
@@ -37,7 +40,7 @@ class EcParams(ctypes.Structure):
     _fields_ = [
         ("B", _i32), ("L", _i32), ("Hq", _i32), ("Hkv", _i32), ("D", _i32), ("V", _i32),
         ("C_max", _i32), ("k", _i32), ("n_dec", _i32), ("tau", _f32), ("logits_dtype", _i32),
-        ("conf_threshold", _f32),
+        ("conf_threshold", _f32), ("scope_lo", _i32), ("scope_hi", _i32),
     ]
 
 
@@ -57,6 +60,7 @@ SIGNATURES: dict[str, tuple] = {
     "ec_entropy_decode": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_entropy_decode_noalloc": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p]),
     "ec_selftest_bounded_wait": (_i32, [_p, ctypes.c_uint64, _p]),
+    "ec_candidates": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p]),
     "ec_lm_head_entropy_workspace_size": (_sz, [_i32]),
     "ec_lm_head_entropy": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_select_recompute": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _p, _p, _p]),

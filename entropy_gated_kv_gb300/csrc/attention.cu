@@ -106,7 +106,7 @@ __device__ __forceinline__ int warp_sum(int v) {
 
 // Whole warp; every warp of every CTA computes the same plan. With no more tiles than
 // clusters, each cluster shares one tile over kCluster key splits; otherwise no split.
-__device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int nclusters) {
+__device__ Plan make_plan(const int32_t* R, int B, int L, int Lk, int Hkv, int nr, int nclusters) {
   const int lane = threadIdx.x & 31;
   int t = 0, r_lane = 0;
   for (int b = lane; b < B; b += 32) {
@@ -118,7 +118,7 @@ __device__ Plan make_plan(const int32_t* R, int B, int L, int Hkv, int nr, int n
   Plan p;
   p.r_lane = r_lane;
   p.tiles = t;
-  p.nkv = (L + kBlockN - 1) / kBlockN;
+  p.nkv = (Lk + kBlockN - 1) / kBlockN;
   const int s = (t > 0 && t <= nclusters) ? min(kCluster, p.nkv) : 1;
   p.bps = (p.nkv + s - 1) / s;
   p.splits = (p.nkv + p.bps - 1) / p.bps;
@@ -134,7 +134,7 @@ __device__ __forceinline__ int cta_item(int k, const Plan& pl, int cluster, int 
 }
 
 // Whole warp. Items are ordered (b, kv head, row tile, split).
-__device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, int L, int Hkv, int nr) {
+__device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, int L, int Lk, int Hkv, int nr) {
   const int lane = threadIdx.x & 31;
   Item it{};
   const int tile = item / pl.splits;
@@ -171,14 +171,14 @@ __device__ Item decode_item(int item, const Plan& pl, const int32_t* R, int B, i
   it.kb0 = it.split * pl.bps;
   const int kb1 = min(pl.nkv, it.kb0 + pl.bps);
   it.nblk = kb1 - it.kb0;
-  it.kv_end = min(L, kb1 * kBlockN);
+  it.kv_end = min(Lk, kb1 * kBlockN);
   return it;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Hq, int Hkv, int g,
+    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ R, int B, int L, int Lk, int Hq, int Hkv, int g,
     int nr, float scale_log2, uint16_t* __restrict__ out, int32_t* __restrict__ dev_err, int plan_early) {
   using LY = Layout<D>;
   // A staged partial row: O as D bf16 (unnormalised; one more rounding than the fp32
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
   // scatter kernel released this one, so the plan is made before the wait (R is read through
   // L2); standalone, R may come from the previous kernel.
   if (!plan_early) pdl_wait();
-  const Plan pl = make_plan(R, B, L, Hkv, nr, nclusters);
+  const Plan pl = make_plan(R, B, L, Lk, Hkv, nr, nclusters);
   if (plan_early) pdl_wait();
   pdl_launch_dependents();
   const bool split_mode = pl.splits > 1;
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     for (int n = 0;; ++n) {
       const int item = cta_item(n, pl, cluster, rank, nclusters);
       if (item < 0) break;
-      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      const Item I = decode_item(item, pl, R, B, L, Lk, Hkv, nr);
       int ok = 1;
       if (lane == 0) {
         if (n > 0) ok = mbar_wait_bounded(&bars->q_empty, (n - 1) & 1, abort_flag, dev_err, kWaitLimitNs);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     for (int n = 0;; ++n) {
       const int item = cta_item(n, pl, cluster, rank, nclusters);
       if (item < 0) break;
-      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      const Item I = decode_item(item, pl, R, B, L, Lk, Hkv, nr);
       int ok = 1;
       if (lane == 0) {
         ok = mbar_wait_bounded(&bars->q_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
     for (int n = 0;; ++n) {
       const int item = cta_item(n, pl, cluster, rank, nclusters);
       if (item < 0) break;
-      const Item I = decode_item(item, pl, R, B, L, Hkv, nr);
+      const Item I = decode_item(item, pl, R, B, L, Lk, Hkv, nr);
       if (split_mode) split_item = I;
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(
       cluster_arrive_release();
       if (got && cluster < pl.tiles) {
         // the tile is shared by the cluster; CTAs without a split of their own decode it here
-        const Item I = split_item.nrows >= 0 ? split_item : decode_item(cluster * pl.splits, pl, R, B, L, Hkv, nr);
+        const Item I = split_item.nrows >= 0 ? split_item : decode_item(cluster * pl.splits, pl, R, B, L, Lk, Hkv, nr);
         constexpr int kCols = D / 4;  // four threads per row, kCols columns each
         const int t = threadIdx.x - 64;
         const int srow = t >> 2;  // row within this CTA's slice
@@ -620,7 +620,10 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
   const cuuint64_t qs[4] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(g) * D * 2,
                             static_cast<cuuint64_t>(p.Hq) * D * 2, static_cast<cuuint64_t>(p.L) * p.Hq * D * 2};
   const cuuint32_t qb[5] = {64, static_cast<cuuint32_t>(g), 1, static_cast<cuuint32_t>(nr), 1};
-  const cuuint64_t kd[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.Hkv), static_cast<cuuint64_t>(p.L),
+  // keys [0, Lk): the whole cache, or up to the end of the gate's scope (block-causal); rows
+  // past Lk read as zeros through the map and are masked out of the softmax
+  const int Lk = scope_hi(p);
+  const cuuint64_t kd[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(p.Hkv), static_cast<cuuint64_t>(Lk),
                             static_cast<cuuint64_t>(p.B)};
   const cuuint64_t ks[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(p.Hkv) * D * 2,
                             static_cast<cuuint64_t>(p.L) * p.Hkv * D * 2};
@@ -670,7 +673,7 @@ cudaError_t launch_impl(const ec_params& p, const void* q, const void* k_cache, 
   }
   cfg.gridDim = dim3(mc * kCluster);
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, tq, tk, tv, R, p.B, p.L, p.Hq, p.Hkv, g, nr, scale * kLog2e,
+  e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, tq, tk, tv, R, p.B, p.L, Lk, p.Hq, p.Hkv, g, nr, scale * kLog2e,
                          static_cast<uint16_t*>(out), dev_err, plan_early ? 1 : 0);
   if (e != cudaSuccess) *status = EC_ERR_CUDA;
   return e;

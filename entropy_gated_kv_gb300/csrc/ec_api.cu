@@ -81,6 +81,8 @@ enum : int { kCheckDecode = 1, kCheckSelect = 2, kCheckAttn = 4 };
 ec_status check_params(const ec_params* p, int what) {
   if (p == nullptr) return EC_ERR_INVALID_ARG;
   if (p->B < 1 || p->B > kMaxB || p->L < 1 || p->L > kMaxL) return EC_ERR_INVALID_ARG;
+  if (has_scope(*p) && !(p->scope_lo >= 0 && p->scope_lo < p->scope_hi && p->scope_hi <= p->L))
+    return EC_ERR_INVALID_ARG;
   if (what & kCheckDecode) {
     if (p->V < 1 || p->V > kMaxV) return EC_ERR_INVALID_ARG;
     if (p->logits_dtype != EC_F32 && p->logits_dtype != EC_BF16) return EC_ERR_INVALID_ARG;
@@ -238,6 +240,18 @@ ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int3
   if (!cand_pos || !cand_count || !ids || !entropy || !log_conf) return EC_ERR_INVALID_ARG;
   return cuda_status(launch_select_recompute(*p, *st, cand_pos, cand_count, ids, entropy, log_conf, false, nullptr,
                                              0, static_cast<cudaStream_t>(stream)));
+}
+
+// ---- candidates for block-wise / sliding-window decoding -----------------------------------------
+ec_status ec_candidates(const ec_params* p, const ec_state* st, int32_t mode, int32_t start, int32_t width,
+                        int32_t* cand_pos, int32_t* cand_count, ec_stream_t stream) {
+  ec_status r = check_params(p, kCheckSelect);
+  if (r != EC_OK) return r;
+  if (st == nullptr || st->mask == nullptr || !cand_pos || !cand_count) return EC_ERR_INVALID_ARG;
+  if (mode != EC_CAND_BLOCK && mode != EC_CAND_SLIDING) return EC_ERR_INVALID_ARG;
+  if (start < 0 || start >= p->L || width < 1 || width > p->C_max) return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_candidates(*p, st->mask, mode, start, width, cand_pos, cand_count,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 // ---- (c) scatter ------------------------------------------------------------------------------

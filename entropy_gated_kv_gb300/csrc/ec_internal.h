@@ -58,6 +58,10 @@ cudaError_t launch_select_recompute(const ec_params& p, const ec_state& st, cons
                                     const float* log_conf, bool prefetch_early, const ChunkPartial* partials,
                                     int32_t nchunks, cudaStream_t s);
 
+// Candidate positions for block-wise / sliding-window decoding (EC_CAND_BLOCK / _SLIDING).
+cudaError_t launch_candidates(const ec_params& p, const uint8_t* mask, int32_t mode, int32_t start, int32_t width,
+                              int32_t* cand_pos, int32_t* cand_count, cudaStream_t s);
+
 // ---- kv_scatter (+ optional query gather) -------------------------------------------------
 cudaError_t launch_kv_scatter(const ec_params& p, void* k_cache, void* v_cache, const void* k_new,
                               const void* v_new, int32_t src_by_position, const int32_t* idx,
@@ -73,6 +77,11 @@ cudaError_t launch_partial_attention(const ec_params& p, const void* q, const vo
                                      int32_t* dev_err, bool plan_early, cudaStream_t s, ec_status* status);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The gate's scope [lo, hi): the whole sequence unless the caller set one (ec_params).
+inline bool has_scope(const ec_params& p) { return p.scope_lo != 0 || p.scope_hi != 0; }
+inline int32_t scope_lo(const ec_params& p) { return has_scope(p) ? p.scope_lo : 0; }
+inline int32_t scope_hi(const ec_params& p) { return has_scope(p) ? p.scope_hi : p.L; }
 
 // ---- per-device launch configuration (ec_api.cu) -------------------------------------------
 // Kernel attributes and device properties apply per device, and the entry points may be

@@ -26,6 +26,10 @@ namespace ec {
 
 struct SelArgs {
   int32_t L, C_max, k, n_dec;
+  // The scope of the gate: positions [scope_lo, scope_hi) (the whole sequence [0, L) unless
+  // the caller decodes block by block). A full step recomputes the scope; a partial step its
+  // masked positions and the recent history entries that lie in it; candidates must lie in it.
+  int32_t scope_lo, scope_hi;
   float tau;
   // confidence-threshold commit: ln(conf_threshold), or -inf for the fixed-count commit
   float log_thresh;
@@ -143,6 +147,13 @@ __device__ __forceinline__ int sel_block_scan(int v, int* total, SelHdr& h) {
 
 __device__ __forceinline__ bool sel_bit(const uint32_t* bm, int p) { return (bm[p >> 5] >> (p & 31)) & 1u; }
 
+// Bits of bitmap word w (positions 32 w .. 32 w + 31) that lie in [lo, hi).
+__device__ __forceinline__ uint32_t sel_scope_bits(int w, int lo, int hi) {
+  const int a = max(lo - 32 * w, 0), b = min(hi - 32 * w, 32);
+  if (b <= a) return 0u;
+  return (b - a == 32 ? 0xFFFFFFFFu : ((1u << (b - a)) - 1u)) << a;
+}
+
 // 32 mask bytes -> one bitmap word (bit t set when byte t is non-zero).
 __device__ __forceinline__ uint32_t sel_bytes_to_bits(uint4 lo, uint4 hi) {
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -204,14 +215,14 @@ __device__ void select_prefetch(const SelArgs& a, int b, uint8_t* dyn) {
     for (int w = tid; w < nwords; w += NT) {
       const uint4 lo = m4[2 * w];
       const uint4 hi = (32 * w + 16 < L) ? m4[2 * w + 1] : make_uint4(0, 0, 0, 0);
-      bitmap[w] = sel_bytes_to_bits(lo, hi);
+      bitmap[w] = sel_bytes_to_bits(lo, hi) & sel_scope_bits(w, a.scope_lo, a.scope_hi);
     }
   } else {
     for (int p0 = warp << 5; p0 < L; p0 += NT) {  // one warp per 32 positions
       const int p = p0 + lane;
       const bool m = p < L && a.mask[rowL + p] != 0;
       const uint32_t bits = __ballot_sync(0xffffffffu, m);
-      if (lane == 0) bitmap[p0 >> 5] = bits;
+      if (lane == 0) bitmap[p0 >> 5] = bits & sel_scope_bits(p0 >> 5, a.scope_lo, a.scope_hi);
     }
   }
   if (k <= kSelMaxRingSmem) {
@@ -358,8 +369,8 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
       if (!full) {
         for (int t = lane; t < count1; t += 32) {  // the last min(k, count) decoded positions
           const int q = rs[((head1 - 1 - t) % k + k) % k];
-          if (q >= 0 && q < L) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
-          else report_error(a.dev_err, EC_DEVERR_BAD_IDX);
+          if (q < 0 || q >= L) report_error(a.dev_err, EC_DEVERR_BAD_IDX);
+          else if (q >= a.scope_lo && q < a.scope_hi) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
         }
         __syncwarp();
         if (nwords <= 32) {  // offsets of each word's bits in idx; every warp writes below
@@ -457,17 +468,18 @@ __device__ void select_finish(const SelArgs& a, int b, uint8_t* dyn) {
       const int head1 = h.head, count1 = h.count;
       for (int t = tid; t < count1; t += NT) {  // the last min(k, count) decoded positions
         const int q = rs[((head1 - 1 - t) % k + k) % k];
-        if (q >= 0 && q < L) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
-        else report_error(a.dev_err, EC_DEVERR_BAD_IDX);
+        if (q < 0 || q >= L) report_error(a.dev_err, EC_DEVERR_BAD_IDX);
+        else if (q >= a.scope_lo && q < a.scope_hi) atomicOr(&bitmap[q >> 5], 1u << (q & 31));
       }
     }
   }
   __syncthreads();
 
   // ---- phase D: the recompute set ------------------------------------------------------------
-  if (h.full) {
-    for (int r = tid; r < L; r += NT) a.idx[rowL + r] = r;
-    if (tid == 0) a.R[b] = L;
+  if (h.full) {  // every position of the scope
+    const int lo = a.scope_lo, n = a.scope_hi - a.scope_lo;
+    for (int r = tid; r < n; r += NT) a.idx[rowL + r] = lo + r;
+    if (tid == 0) a.R[b] = n;
     return;
   }
   if (fast && nwords <= 32) {

@@ -25,7 +25,65 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(SelArgs a) {
   select_finish<kThreads>(a, blockIdx.x, dyn);
 }
 
+// Candidates of a step for block-wise or sliding-window decoding, one CTA per sequence: the
+// masked positions of the window [w0, w0 + width), ascending. Block mode: w0 = start.
+// Sliding mode: w0 = the first masked position at or after start (L if none).
+constexpr int kCandThreads = 256;
+
+__global__ void __launch_bounds__(kCandThreads) candidates_kernel(const uint8_t* __restrict__ mask, int L, int C_max,
+                                                                  int mode, int start, int width,
+                                                                  int32_t* __restrict__ cand_pos,
+                                                                  int32_t* __restrict__ cand_count) {
+  __shared__ int first;
+  __shared__ int warp_n[kCandThreads / 32];
+  __shared__ int carry;
+  pdl_wait();  // the mask comes from the previous step's select kernel
+  pdl_launch_dependents();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint8_t* m = mask + static_cast<int64_t>(b) * L;
+  int w0 = start;
+  if (mode == EC_CAND_SLIDING) {
+    if (tid == 0) first = L;
+    __syncthreads();
+    for (int p0 = start; p0 < L; p0 += kCandThreads) {
+      const int p = p0 + tid;
+      const bool hit = p < L && m[p] != 0;
+      if (hit) atomicMin(&first, p);
+      if (__syncthreads_or(hit)) break;
+    }
+    w0 = first;
+  }
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  const int hi = min(L, w0 + width);
+  int32_t* out = cand_pos + static_cast<int64_t>(b) * C_max;
+  for (int p0 = w0; p0 < hi; p0 += kCandThreads) {  // compaction, ascending
+    const int p = p0 + tid;
+    const bool hit = p < hi && m[p] != 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) warp_n[warp] = __popc(bal);
+    __syncthreads();
+    int before = carry, tot = 0;
+    for (int w = 0; w < kCandThreads / 32; ++w) {
+      if (w < warp) before += warp_n[w];
+      tot += warp_n[w];
+    }
+    if (hit) out[before + __popc(bal & ((1u << lane) - 1u))] = p;
+    __syncthreads();
+    if (tid == 0) carry += tot;
+    __syncthreads();
+  }
+  for (int i = carry + tid; i < C_max; i += kCandThreads) out[i] = -1;
+  if (tid == 0) cand_count[b] = carry;
+}
+
 }  // namespace
+
+cudaError_t launch_candidates(const ec_params& p, const uint8_t* mask, int32_t mode, int32_t start, int32_t width,
+                              int32_t* cand_pos, int32_t* cand_count, cudaStream_t s) {
+  return launch_pdl(candidates_kernel, dim3(p.B), dim3(kCandThreads), 0, s, mask, p.L, p.C_max, mode, start, width,
+                    cand_pos, cand_count);
+}
 
 SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* cand_pos, const int32_t* cand_count,
                       const int32_t* ids, const float* entropy, const float* log_conf, bool prefetch_early,
@@ -35,6 +93,8 @@ SelArgs make_sel_args(const ec_params& p, const ec_state& st, const int32_t* can
   a.partials = partials;
   a.nchunks = nchunks;
   a.L = p.L;
+  a.scope_lo = scope_lo(p);
+  a.scope_hi = scope_hi(p);
   a.C_max = p.C_max;
   a.k = p.k;
   a.n_dec = p.n_dec;

@@ -92,12 +92,26 @@ typedef void* ec_stream_t; /* a cudaStream_t */
  *        open — of those n_dec, only the candidates whose decode confidence p(id) is at least
  *        conf_threshold are committed, and the single most confident one when none is. A
  *        zero-initialised struct gets the fixed-count commit.
+ * scope_lo, scope_hi  the gate's scope, the same for every sequence of the call. Both 0: the
+ *        whole sequence [0, L) (the EntropyCache step as the pages state it). Otherwise
+ *        0 <= scope_lo < scope_hi <= L: block-by-block decoding (block diffusion) with the
+ *        gate as a sub-block recompute signal, a use the pages name for the gate (zh summary
+ *        §5 "通用性潜力"; pt summary §5 "Generalidade"). The block being decoded is
+ *        [scope_lo, scope_hi) and the blocks after it do not exist yet, so:
+ *          - candidates must lie in the scope (others are dropped, EC_DEVERR_BAD_CAND_POS);
+ *          - a full step recomputes the scope: idx = scope_lo .. scope_hi - 1;
+ *          - a partial step recomputes the scope's masked positions and those of the last
+ *            min(k, count) history entries that lie in the scope;
+ *          - attention reads the keys [0, scope_hi) only (block-causal: the block and every
+ *            block before it).
+ *        A zero-initialised struct gets the whole-sequence gate.
  */
 typedef struct ec_params {
   int32_t B, L, Hq, Hkv, D, V, C_max, k, n_dec;
   float tau;
   int32_t logits_dtype;
   float conf_threshold;
+  int32_t scope_lo, scope_hi;
 } ec_params;
 
 /* ---- per-sequence decode state (all device arrays, caller-owned) ----------------------
@@ -244,6 +258,25 @@ ec_status ec_lm_head_entropy(const void* hidden, const void* weight, int32_t n_r
 ec_status ec_select_recompute(const ec_params* p, const ec_state* st, const int32_t* cand_pos,
                               const int32_t* cand_count, const int32_t* ids,
                               const float* entropy, const float* log_conf, ec_stream_t stream);
+
+/* ---- candidates for block-wise and sliding-window decoding -------------------------------
+ * The pages note that the entropy gate carries over to other decoding strategies, such as
+ * sliding-window and block decoding (pt summary §5 "Generalidade"; zh summary §5). A step's
+ * candidates (the rows whose logits it decodes: cand_pos / cand_count of ec_step) are the
+ * masked positions of the window being decoded; this builds them on the device from
+ * st->mask, so that a multi-step decoding loop needs no host round trip. Per sequence b:
+ *   EC_CAND_BLOCK    window [start, start + width): the block starting at `start`;
+ *   EC_CAND_SLIDING  window [f, f + width), f = the first masked position at or after
+ *                    `start` (L if none): a window that slides forward as its earliest
+ *                    position is decoded;
+ *   cand_pos[b, 0 .. n-1] = the masked positions of the window (clipped to [0, L)),
+ *   ascending; cand_pos[b, n .. C_max-1] = -1; cand_count[b] = n.
+ * 0 <= start < L, 1 <= width <= C_max. cand_pos int32 [B, C_max], cand_count int32 [B]
+ * (device). Only st->mask is read. */
+#define EC_CAND_BLOCK 0
+#define EC_CAND_SLIDING 1
+ec_status ec_candidates(const ec_params* p, const ec_state* st, int32_t mode, int32_t start, int32_t width,
+                        int32_t* cand_pos, int32_t* cand_count, ec_stream_t stream);
 
 /* ---- (c) K/V cache refresh ---------------------------------------------------------------
  * Recomputed positions receive fresh K/V, all other positions keep their cached rows

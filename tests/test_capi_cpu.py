@@ -211,3 +211,31 @@ def test_conf_threshold_validation(capi):
     for bad in (math.nan, 1.5):
         p = _params(capi, conf_threshold=bad)
         assert lib.ec_step_workspace_size(ctypes.byref(p)) == 0, bad
+
+
+def test_scope_validation(capi):
+    lib = capi.load()
+    # both 0: the whole sequence; otherwise 0 <= lo < hi <= L
+    for lo, hi in ((0, 0), (0, 1024), (992, 1024), (0, 32), (5, 6)):
+        p = _params(capi, scope_lo=lo, scope_hi=hi)
+        assert lib.ec_step_workspace_size(ctypes.byref(p)) > 0, (lo, hi)
+    for lo, hi in ((-1, 32), (32, 32), (40, 32), (0, 1025), (1024, 1025), (7, 0)):
+        p = _params(capi, scope_lo=lo, scope_hi=hi)
+        assert lib.ec_step_workspace_size(ctypes.byref(p)) == 0, (lo, hi)
+
+
+def test_candidates_validation(capi):
+    lib = capi.load()
+    INV = capi.EC_ERR_INVALID_ARG
+    p = _params(capi)
+    st = capi.EcState(*([1 << 20] * 11))  # never dereferenced: validation fails first
+    buf = ctypes.c_void_p(1 << 20)
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 2, 0, 32, buf, buf, None) == INV  # bad mode
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 0, -1, 32, buf, buf, None) == INV  # start < 0
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 0, 1024, 32, buf, buf, None) == INV  # start >= L
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 1, 0, 0, buf, buf, None) == INV  # width < 1
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 1, 0, 33, buf, buf, None) == INV  # width > C_max
+    assert lib.ec_candidates(ctypes.byref(p), None, 0, 0, 32, buf, buf, None) == INV
+    assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 0, 0, 32, None, buf, None) == INV
+    bad = _params(capi, scope_lo=3, scope_hi=2)
+    assert lib.ec_candidates(ctypes.byref(bad), ctypes.byref(st), 0, 0, 32, buf, buf, None) == INV

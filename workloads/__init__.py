@@ -22,6 +22,8 @@ Logit distributions:
   gauss_scale  row i ~ N(0, s_i^2), s_i ~ U[0.5, 8]
   zipf         per row a random permutation gives every token a rank rho in 1..V and
                logit = -1.1 ln rho + N(0, 1)
+  schedule     as trace, with the peak heights 17.75 - 0.125 pi(i) for a seeded permutation
+               pi of the rows (block-wise and sliding-window decoding tests)
   trace        per (step, sequence) a Bernoulli(0.1) draw (step 0 always high) picks
                high: every row N(0, 0.5^2)  (entropy about ln V)
                low:  every row N(0, 1) except one seeded token set to a peak; with c
@@ -216,6 +218,18 @@ def step_logits(w: Workload, step: int = 0) -> np.ndarray:
             for i in range(C):
                 rank = r.permutation(V).astype(np.float32) + np.float32(1.0)
                 out[b, i] = np.float32(-1.1) * np.log(rank) + r.standard_normal(V, dtype=np.float32)
+        elif w.logits_kind == "schedule":
+            # as "trace", but the peak heights 17.75 - 0.125 pi(i) (exact in bf16) follow a
+            # seeded permutation pi of the rows, so that the most confident candidate is
+            # anywhere in the window, not always the last row. At V = 32000 the best row has
+            # entropy below 0.7 and its confidence leads the next one by more than 1e-4 in log
+            if trace_is_high(w, step, b):
+                out[b] = r.standard_normal((C, V), dtype=np.float32) * np.float32(0.5)
+            else:
+                out[b] = r.standard_normal((C, V), dtype=np.float32)
+                peak = r.integers(0, V, size=C)
+                height = 17.75 - 0.125 * r.permutation(C)
+                out[b, np.arange(C), peak] = height.astype(np.float32)
         elif w.logits_kind == "trace":
             if trace_is_high(w, step, b):
                 out[b] = r.standard_normal((C, V), dtype=np.float32) * np.float32(0.5)

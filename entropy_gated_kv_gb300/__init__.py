@@ -131,7 +131,7 @@ class DecodeState:
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
-    """Zero-filled scratch buffer (the library keeps its counters at zero between calls)."""
+    """Scratch buffer for an entry point's workspace (the library needs no initial contents)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 

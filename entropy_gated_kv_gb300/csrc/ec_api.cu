@@ -206,10 +206,9 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
   if (!logits || !ids || !entropy || !log_conf || !aligned16(logits)) return EC_ERR_INVALID_ARG;
   if (static_cast<int64_t>(n_rows) * entropy_num_chunks(V, dtype) > INT32_MAX) return EC_ERR_UNSUPPORTED;
   const size_t need = entropy_workspace_bytes(n_rows, V, dtype);
-  if (entropy_num_chunks(V, dtype) > 1 && (ws == nullptr || ws_bytes < need || !aligned16(ws)))
-    return EC_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return EC_ERR_INVALID_ARG;
   return cuda_status(launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf, ws,
-                                           nullptr, 1, true, false, nullptr, static_cast<cudaStream_t>(stream)));
+                                           nullptr, 1, true, false, static_cast<cudaStream_t>(stream)));
 }
 
 // ---- (a) from the hidden states ----------------------------------------------------------------
@@ -326,7 +325,7 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
 
   // stages (a)-(c): decode + entropy of the candidate rows, then the select stage
   cudaError_t e = launch_entropy_decode(logits, p->V, p->B * p->C_max, p->V, p->logits_dtype, ids, ent, conf,
-                                        w + lay.k1, cand_count, p->C_max, false, true, st->dev_err, s);
+                                        w + lay.k1, cand_count, p->C_max, false, true, s);
   // the decode kernel waits for every earlier kernel before it releases this one, so the select
   // kernel may stage the state before its own wait
   if (e == cudaSuccess)

@@ -11,8 +11,9 @@
 namespace ec {
 
 // ---- entropy_decode ---------------------------------------------------------------------
-// Partial result of one vocabulary chunk of one row: raw max logit, its (lowest) index, and
-// S = sum 2^d, T = sum d 2^d with d = (x - max) * log2(e).
+// Partial result of one piece of one row (entropy_decode.cu: 1024 bf16 or 512 fp32
+// elements): raw max logit, its (lowest) index, and S = sum 2^d, T = sum d 2^d with
+// d = (x - max) * log2(e).
 struct ChunkPartial {
   float m;
   int32_t idx;
@@ -20,22 +21,20 @@ struct ChunkPartial {
   float t;
 };
 
-int entropy_chunk_elems(int32_t dtype);
+// Pieces per row: the partials per row that a publishing launch writes to the workspace.
 int32_t entropy_num_chunks(int32_t V, int32_t dtype);
 size_t entropy_workspace_bytes(int32_t n_rows, int32_t V, int32_t dtype);
 // row_count (may be null): rows r with (r % rows_per_group) >= row_count[r / rows_per_group]
 // are skipped (their outputs are left untouched). allow_cluster: few rows may take the
-// one-cluster-per-row launch (lowest latency on an idle GPU); without it, or with many rows,
-// the one-CTA-per-chunk launch runs, whose small independent CTAs become resident while a
-// large predecessor kernel is still running (the better choice inside a chain of kernels).
-// publish_only: the chunk partials (max, index, S, T) are written to the workspace and the
-// next kernel merges them (ids / entropy / log_conf are not written). Outside publish-only
-// mode, problems of 32 MB and more stream through persistent CTAs (same workspace layout).
-// dev_err (may be null): where a timed-out wait of the streaming path is reported.
+// one-cluster-per-row launch, which merges on chip (lowest latency on an idle GPU); without
+// it, or with many rows, the split launch (or, from 32 MB, the pipelined one) publishes one
+// partial per piece to the workspace and a merge kernel writes the rows. publish_only: the
+// partials are left in the workspace for the next kernel to merge (ids / entropy / log_conf
+// are not written). No workspace contents need to be initialised.
 cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                   int32_t dtype, int32_t* ids, float* entropy, float* log_conf, void* ws,
                                   const int32_t* row_count, int32_t rows_per_group, bool allow_cluster,
-                                  bool publish_only, int32_t* dev_err, cudaStream_t s);
+                                  bool publish_only, cudaStream_t s);
 
 // ---- output projection fused with the decode (lm_head_entropy.cu) -------------------------
 size_t lm_head_workspace_bytes(int32_t n_rows);

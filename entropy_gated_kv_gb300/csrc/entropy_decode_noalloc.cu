@@ -11,8 +11,9 @@
 // The array (EC_NOALLOC_SCRATCH_BYTES) exists on every GPU that loads the library and stays
 // there until the process exits. Its device address is looked up once per device, on the
 // first call made with that device current. Every call shares it and it keeps the last
-// call's contents: each call clears the merge counters it needs on its own stream before the
-// kernel, and calls that overlap on the GPU race with each other.
+// call's contents; no call needs it to start in any particular state (every partial result a
+// call reads back is one it wrote first), and calls that overlap on the GPU race with each
+// other.
 #include <mutex>
 
 #include "ec_internal.h"
@@ -21,7 +22,7 @@ namespace {
 
 constexpr size_t kScratchBytes = EC_NOALLOC_SCRATCH_BYTES;
 
-// The scratch: partial results per (row, vocabulary chunk), then one counter per row.
+// The scratch: one partial result per (row, vocabulary piece).
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
@@ -66,14 +67,7 @@ extern "C" ec_status ec_entropy_decode_noalloc(const void* logits, int64_t row_s
   void* scratch = nullptr;
   if (scratch_for_current_device(&scratch) != cudaSuccess) return EC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (nch > 1) {
-    // The row counters must start at zero; the array holds whatever the last call left.
-    const size_t rows = static_cast<size_t>(n_rows);
-    const size_t counters = ec::align_up(rows * nch * sizeof(ec::ChunkPartial), 256);
-    if (cudaMemsetAsync(static_cast<char*>(scratch) + counters, 0, rows * sizeof(uint32_t), s) != cudaSuccess)
-      return EC_ERR_CUDA;
-  }
   const cudaError_t e = ec::launch_entropy_decode(logits, row_stride, n_rows, V, dtype, ids, entropy, log_conf,
-                                                  scratch, nullptr, 1, true, false, nullptr, s);
+                                                  scratch, nullptr, 1, true, false, s);
   return e == cudaSuccess ? EC_OK : EC_ERR_CUDA;
 }

@@ -176,8 +176,7 @@ int32_t ec_version(void);
  *            each row are read. row_stride >= V and row_stride * elem_size % 16 == 0.
  * ids        int32 [n_rows]; entropy, log_conf fp32 [n_rows].
  * ws         workspace of at least ec_entropy_decode_workspace_size(n_rows, V, dtype)
- *            bytes; it must be zero-filled before its first use and the library leaves it
- *            ready for the next call (its counters return to zero). Calls that share a
+ *            bytes (16-byte aligned); no initial contents are needed. Calls that share a
  *            workspace must not overlap in time.
  * Accumulation is fp32; argmax compares the raw stored values, so ids are exact. -inf
  * logits contribute zero probability. NaN logits are not supported (results undefined).
@@ -203,10 +202,10 @@ ec_status ec_entropy_decode(const void* logits, int64_t row_stride, int32_t n_ro
  * with that device current): make that first call before any stream capture. The address is
  * kept for the life of the process; cudaDeviceReset() on a device invalidates it, so do not
  * call this entry point on a device after resetting it.
- * Every call shares the one array, which keeps the last call's contents; each call clears the
- * counters it needs with an asynchronous memset on `stream` before its kernel. Calls whose
- * executions overlap on the GPU (other streams, other host threads) race and give wrong
- * results: order them. No cudaMalloc, cudaFree or allocating library routine is called. */
+ * Every call shares the one array, which keeps the last call's contents; no call needs it to
+ * start in any particular state (every partial result a call reads is one it wrote first).
+ * Calls whose executions overlap on the GPU (other streams, other host threads) race and give
+ * wrong results: order them. No cudaMalloc, cudaFree or allocating library routine is called. */
 #define EC_NOALLOC_SCRATCH_BYTES (1u << 20)
 ec_status ec_entropy_decode_noalloc(const void* logits, int64_t row_stride, int32_t n_rows, int32_t V,
                                     int32_t dtype, int32_t* ids, float* entropy, float* log_conf,
@@ -328,7 +327,7 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
  * call's attention stage, which stands for the next forward pass of the workflow.
  * The pointer arrays k_cache ... out are HOST arrays of n_layers device pointers.
  * cand_pos, cand_count: as for ec_select_recompute.
- * ws at least ec_step_workspace_size(p) bytes, zero-filled before its first use.
+ * ws at least ec_step_workspace_size(p) bytes (16-byte aligned, no initial contents needed).
  * scale as for ec_partial_attention. */
 size_t ec_step_workspace_size(const ec_params* p);
 ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits,

@@ -52,6 +52,10 @@ __all__ = [
     "sliding_window_candidates",
     "kv_scatter",
     "attention",
+    "rms_norm",
+    "rope",
+    "swiglu",
+    "layer_forward",
     "step",
 ]
 
@@ -265,6 +269,76 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.n
         w = w / w.sum(axis=1, keepdims=True)
         out[:, h, :] = w @ v[:, kv, :]
     return out
+
+
+# --------------------------------------------------------------------------------------
+# the partial forward of one transformer layer  —  [zh] §2.2 "前向传播 / 部分传播": only the
+# recompute set is recomputed, every other position is read from the K/V cache. The layer is
+# the LLaMA-style block of the evaluated models (RMSNorm, rotary position embedding,
+# grouped-query attention, SwiGLU feed-forward); the pages name the models, not their layers,
+# so this is the plainest reading of "a forward pass" of them.
+
+
+def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """Root-mean-square normalisation over the last axis, then a per-feature gain:
+    x / sqrt(mean(x^2) + eps) * gamma."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, dtype=np.float64)
+
+
+def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary position embedding of x [R, H, D] at positions pos [R], rotate-half pairing:
+    feature i and i + D/2 form a pair rotated by the angle pos * theta^(-2i/D), i < D/2."""
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    h = D // 2
+    inv = np.asarray(theta, dtype=np.float64) ** (-2.0 * np.arange(h, dtype=np.float64) / D)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * inv[None, :]  # [R, D/2]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    a, b = x[..., :h], x[..., h:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """SiLU(g) * u with SiLU(g) = g / (1 + exp(-g))."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g)) * np.asarray(u, dtype=np.float64)
+
+
+def layer_forward(*, x_src: np.ndarray, idx: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                  weights: dict, Hq: int, Hkv: int, theta: float, eps: float,
+                  rows: np.ndarray | None = None) -> dict:
+    """Partial forward of one layer for the recompute rows idx of one sequence, in float64.
+
+    x_src [L, d]: the layer input at every position; k_cache, v_cache [L, Hkv, D]; weights:
+    wq [Hq D, d], wk, wv [Hkv D, d], wo [d, Hq D], wg, wu [d_ff, d], wd [d, d_ff], gamma1,
+    gamma2 [d]. For every recompute row r (position idx[r]):
+      x = x_src[idx], h = rms_norm(x, gamma1)
+      q, k, v = h wq^T, h wk^T, h wv^T; q, k rotated at their positions (rope)
+      the cache rows at idx take k and v (the K/V refresh of the recompute set)
+      o = attention of q against the whole refreshed cache (unmasked, scale 1/sqrt(D))
+      x2 = x + o wo^T;  y = x2 + swiglu(h2 wg^T, h2 wu^T) wd^T with h2 = rms_norm(x2, gamma2)
+    rows: compute o, x2 and y for these recompute rows only (a sample); q, k, v and the caches
+    are always complete.
+    """
+    W = {n: np.asarray(a, dtype=np.float64) for n, a in weights.items()}
+    idx = np.asarray(idx, dtype=np.int64)
+    R = idx.shape[0]
+    D = k_cache.shape[-1]
+    x = np.asarray(x_src, dtype=np.float64)[idx]
+    h = rms_norm(x, W["gamma1"], eps)
+    q = rope((h @ W["wq"].T).reshape(R, Hq, D), idx, theta)
+    k = rope((h @ W["wk"].T).reshape(R, Hkv, D), idx, theta)
+    v = (h @ W["wv"].T).reshape(R, Hkv, D)
+    kc = kv_scatter(np.asarray(k_cache, dtype=np.float64), idx, k)
+    vc = kv_scatter(np.asarray(v_cache, dtype=np.float64), idx, v)
+    sel = np.arange(R) if rows is None else np.asarray(rows, dtype=np.int64)
+    o = attention(q[sel], kc, vc, 1.0 / math.sqrt(D))
+    x2 = x[sel] + o.reshape(len(sel), Hq * D) @ W["wo"].T
+    h2 = rms_norm(x2, W["gamma2"], eps)
+    y = x2 + swiglu(h2 @ W["wg"].T, h2 @ W["wu"].T) @ W["wd"].T
+    return {"q": q, "k": k, "v": v, "k_cache": kc, "v_cache": vc, "o": o, "x2": x2, "y": y, "rows": sel}
 
 
 # --------------------------------------------------------------------------------------

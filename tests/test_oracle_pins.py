@@ -518,3 +518,151 @@ def test_scoped_step_brute_force_and_block_causal_attention():
     vc[lo:hi] = lay["v_src"][lo:hi]
     want = _sdpa(lay["q_src"][lo:hi], kc[:hi], vc[:hi], 1.0 / math.sqrt(D))
     np.testing.assert_allclose(got["layers"][0]["out"], want, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------------------
+# the partial forward of one layer ([zh] §2.2 partial forward): RMSNorm, RoPE, SwiGLU, the block
+
+
+def test_rms_norm_closed_forms():
+    np.testing.assert_allclose(O.rms_norm(np.array([3.0, 4.0]), np.ones(2), 0.0),
+                               [3.0 / math.sqrt(12.5), 4.0 / math.sqrt(12.5)], rtol=1e-15)
+    c = np.full(7, -2.5)
+    gamma = np.arange(1.0, 8.0)
+    np.testing.assert_allclose(O.rms_norm(c, gamma, 0.0), -gamma, rtol=1e-15)  # a constant row: its sign times gamma
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal((5, 64))
+    y = O.rms_norm(x, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, rtol=1e-14)  # unit RMS
+    np.testing.assert_allclose(O.rms_norm(3.7 * x, np.ones(64), 0.0), y, rtol=1e-14)  # scale invariance
+    assert abs(O.rms_norm(np.array([1e-3]), np.ones(1), 1e-6)[0] - 1e-3 / math.sqrt(1e-6 + 1e-6)) < 1e-15  # eps
+
+
+def test_rope_closed_forms_and_invariants():
+    # D = 2: (1, 0) at position p is (cos p, sin p); D = 4: the second pair turns by p theta^(-1/2)
+    for p in (0, 1, 5, 1000):
+        np.testing.assert_allclose(O.rope(np.array([[[1.0, 0.0]]]), np.array([p]), 10000.0)[0, 0],
+                                   [math.cos(p), math.sin(p)], atol=1e-12)
+    x = np.array([[[0.0, 2.0, 0.0, 0.0]]])  # feature 1 pairs with feature 3
+    a = 7 * 100.0 ** -0.5
+    np.testing.assert_allclose(O.rope(x, np.array([7]), 100.0)[0, 0], [0.0, 2 * math.cos(a), 0.0, 2 * math.sin(a)],
+                               atol=1e-12)
+    rng = np.random.default_rng(52)
+    q = rng.standard_normal((1, 3, 16))
+    k = rng.standard_normal((1, 3, 16))
+    np.testing.assert_allclose(O.rope(q, np.array([0]), 500000.0), q, atol=0)  # position 0: identity
+    r = O.rope(q, np.array([123]), 500000.0)
+    np.testing.assert_allclose(np.linalg.norm(r[..., :8] ** 2 + r[..., 8:] ** 2),
+                               np.linalg.norm(q[..., :8] ** 2 + q[..., 8:] ** 2), rtol=1e-12)  # pair norms kept
+    # relative positions: <rope(q, m), rope(k, n)> depends on m - n only
+    for m, n, t in ((5, 2, 40), (100, 300, 7)):
+        a1 = np.sum(O.rope(q, np.array([m]), 10000.0) * O.rope(k, np.array([n]), 10000.0), axis=-1)
+        a2 = np.sum(O.rope(q, np.array([m + t]), 10000.0) * O.rope(k, np.array([n + t]), 10000.0), axis=-1)
+        np.testing.assert_allclose(a1, a2, rtol=1e-10, atol=1e-12)
+
+
+def test_swiglu_closed_forms():
+    assert O.swiglu(np.array([0.0]), np.array([5.0]))[0] == 0.0
+    assert abs(O.swiglu(np.array([1.0]), np.array([2.0]))[0] - 2.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(O.swiglu(np.array([40.0]), np.array([3.0]))[0] - 120.0) < 1e-12  # SiLU(g) -> g
+    assert abs(O.swiglu(np.array([-40.0]), np.array([3.0]))[0]) < 1e-15  # SiLU(g) -> 0
+
+
+def _layer_weights(rng, d, Hq, Hkv, D, dff, scale=1.0):
+    return {"wq": rng.standard_normal((Hq * D, d)) * scale, "wk": rng.standard_normal((Hkv * D, d)) * scale,
+            "wv": rng.standard_normal((Hkv * D, d)) * scale, "wo": rng.standard_normal((d, Hq * D)) * scale,
+            "wg": rng.standard_normal((dff, d)) * scale, "wu": rng.standard_normal((dff, d)) * scale,
+            "wd": rng.standard_normal((d, dff)) * scale, "gamma1": 1.0 + 0.1 * rng.standard_normal(d),
+            "gamma2": 1.0 + 0.1 * rng.standard_normal(d)}
+
+
+def _brute_layer(x_src, idx, kc0, vc0, W, Hq, Hkv, D, theta, eps):
+    """Index-by-index restatement of the layer (explicit sums over (output, input) weight
+    indices), for tiny shapes."""
+    L, d = len(x_src), len(x_src[0])
+    dff = len(W["wg"])
+    g = Hq // Hkv
+
+    def norm(v, gam):
+        ms = sum(t * t for t in v) / len(v)
+        return [v[i] / math.sqrt(ms + eps) * gam[i] for i in range(len(v))]
+
+    def mat(Wm, v):  # (W v)_j = sum_i W[j][i] v[i]
+        return [sum(Wm[j][i] * v[i] for i in range(len(v))) for j in range(len(Wm))]
+
+    def rot(vec, pos):  # one head
+        h = D // 2
+        out = list(vec)
+        for i in range(h):
+            ang = pos * theta ** (-2.0 * i / D)
+            out[i] = vec[i] * math.cos(ang) - vec[i + h] * math.sin(ang)
+            out[i + h] = vec[i + h] * math.cos(ang) + vec[i] * math.sin(ang)
+        return out
+
+    kc = [[list(kc0[p][j]) for j in range(Hkv)] for p in range(L)]
+    vc = [[list(vc0[p][j]) for j in range(Hkv)] for p in range(L)]
+    qs, hs, xs = [], [], []
+    for p in idx:
+        x = list(x_src[p])
+        h = norm(x, W["gamma1"])
+        q, k, v = mat(W["wq"], h), mat(W["wk"], h), mat(W["wv"], h)
+        qs.append([rot(q[a * D:(a + 1) * D], p) for a in range(Hq)])
+        kc[p] = [rot(k[a * D:(a + 1) * D], p) for a in range(Hkv)]
+        vc[p] = [v[a * D:(a + 1) * D] for a in range(Hkv)]
+        xs.append(x)
+    ys = []
+    for r, p in enumerate(idx):
+        o = []
+        for a in range(Hq):
+            s = [sum(qs[r][a][e] * kc[j][a // g][e] for e in range(D)) / math.sqrt(D) for j in range(L)]
+            m = max(s)
+            w = [math.exp(t - m) for t in s]
+            z = sum(w)
+            o.extend(sum(w[j] / z * vc[j][a // g][e] for j in range(L)) for e in range(D))
+        x2 = [xs[r][i] + t for i, t in enumerate(mat(W["wo"], o))]
+        h2 = norm(x2, W["gamma2"])
+        gg, uu = mat(W["wg"], h2), mat(W["wu"], h2)
+        act = [gg[j] / (1 + math.exp(-gg[j])) * uu[j] for j in range(dff)]
+        ys.append([x2[i] + t for i, t in enumerate(mat(W["wd"], act))])
+    return np.array(ys), np.array(kc), np.array(vc)
+
+
+def test_layer_forward_brute_force_tiny():
+    rng = np.random.default_rng(53)
+    for trial in range(6):
+        L, d, Hq, Hkv, D, dff = 6, 4, 2, (1, 2)[trial % 2], 2, 3
+        x_src = rng.standard_normal((L, d))
+        kc = rng.standard_normal((L, Hkv, D))
+        vc = rng.standard_normal((L, Hkv, D))
+        W = _layer_weights(rng, d, Hq, Hkv, D, dff, scale=0.5)
+        idx = np.sort(rng.choice(L, size=int(rng.integers(1, L + 1)), replace=False))
+        got = O.layer_forward(x_src=x_src, idx=idx, k_cache=kc, v_cache=vc, weights=W, Hq=Hq, Hkv=Hkv,
+                              theta=10.0, eps=1e-5)
+        y, kc2, vc2 = _brute_layer(x_src, idx, kc, vc, W, Hq, Hkv, D, 10.0, 1e-5)
+        np.testing.assert_allclose(got["y"], y, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(got["k_cache"], kc2, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(got["v_cache"], vc2, rtol=1e-12, atol=1e-14)
+
+
+def test_layer_forward_residual_paths_and_sampled_rows():
+    rng = np.random.default_rng(54)
+    L, d, Hq, Hkv, D, dff = 9, 8, 2, 2, 4, 6
+    x_src = rng.standard_normal((L, d))
+    kc = rng.standard_normal((L, Hkv, D))
+    vc = rng.standard_normal((L, Hkv, D))
+    W = _layer_weights(rng, d, Hq, Hkv, D, dff)
+    idx = np.array([1, 4, 5, 8])
+    # zero output projections: both residual paths carry x through unchanged
+    Z = dict(W, wo=np.zeros_like(W["wo"]), wd=np.zeros_like(W["wd"]))
+    got = O.layer_forward(x_src=x_src, idx=idx, k_cache=kc, v_cache=vc, weights=Z, Hq=Hq, Hkv=Hkv, theta=100.0,
+                          eps=1e-6)
+    np.testing.assert_allclose(got["y"], x_src[idx], rtol=0, atol=0)
+    # a sample of rows gives the same rows as the whole set
+    full = O.layer_forward(x_src=x_src, idx=idx, k_cache=kc, v_cache=vc, weights=W, Hq=Hq, Hkv=Hkv, theta=100.0,
+                           eps=1e-6)
+    part = O.layer_forward(x_src=x_src, idx=idx, k_cache=kc, v_cache=vc, weights=W, Hq=Hq, Hkv=Hkv, theta=100.0,
+                           eps=1e-6, rows=np.array([2, 0]))
+    np.testing.assert_allclose(part["y"], full["y"][[2, 0]], rtol=1e-14)
+    # the recomputed rows' attention reads the refreshed cache rows (not the stale ones)
+    assert not np.allclose(full["k_cache"][idx], kc[idx])
+    np.testing.assert_array_equal(full["k_cache"][[0, 2, 3, 6, 7]], kc[[0, 2, 3, 6, 7]])

@@ -601,6 +601,75 @@ def run_trace(E, dev, n_steps) -> dict:
     }
 
 
+def run_layer_forward(E, dev, n_steps) -> dict:
+    """The partial forward of one LLaDA-8B-shaped layer (d 4096, 32 x 128 MHA, d_ff 12288, L 1024)
+    for the headline step's recompute set (R = 95), against the full forward (R = L): the time
+    per layer of the forward each flag selects, and its roofline (weight bytes for the partial
+    forward, tensor-core flops for the full one). Weights drawn on the device at the usual
+    initialisation scale; graph-replayed."""
+    import torch
+
+    w = W.workload(2)
+    d, dff, L = w.Hq * w.D, 12288, w.L
+    p = params_of(E, w)
+    g = torch.Generator(device=dev).manual_seed(7)
+    bf = torch.bfloat16
+
+    def mat(r, c):
+        return (torch.randn(r, c, generator=g, device=dev) / c ** 0.5).to(bf)
+
+    cs, sn = E.rope_table(L, w.D, 500000.0, device=dev)
+    lw = E.LayerWeights(wq=mat(d, d), wk=mat(w.Hkv * w.D, d), wv=mat(w.Hkv * w.D, d), wo=mat(d, d),
+                        wg=mat(dff, d), wu=mat(dff, d), wd=mat(d, dff),
+                        gamma1=(1 + 0.1 * torch.randn(d, generator=g, device=dev)).to(bf),
+                        gamma2=(1 + 0.1 * torch.randn(d, generator=g, device=dev)).to(bf), rope_cos=cs, rope_sin=sn)
+    x_src = torch.randn(1, L, d, generator=g, device=dev).to(bf)
+    kc = torch.randn(1, L, w.Hkv, w.D, generator=g, device=dev).to(bf)
+    vc = torch.randn(1, L, w.Hkv, w.D, generator=g, device=dev).to(bf)
+    # the headline step's recompute set, from the library's own select stage
+    st_h = W.snapshot_state(w)
+    base, _, _ = host_inputs(w, dev)
+    st = E.DecodeState.from_arrays(p, device=dev, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
+                                   ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
+    E.step(p, st, base["logits"], torch.from_numpy(st_h["cand_pos"]).to(dev),
+           torch.from_numpy(st_h["cand_count"]).to(dev), [], ws=E.workspace(E.step_workspace_size(p), dev))
+    torch.cuda.synchronize()
+    del base
+    ws = E.workspace(E.layer_forward_workspace_size(p, dff), dev)
+    y = torch.empty(1, L, d, dtype=bf, device=dev)
+    out = {}
+    full_idx = torch.arange(L, dtype=torch.int32, device=dev).view(1, L)
+    for name, idx, R in (("partial", st.idx, st.R), ("full", full_idx, torch.tensor([L], dtype=torch.int32, device=dev))):
+        n = n_steps if name == "partial" else max(10, n_steps // 8)
+        E.layer_forward(p, lw, idx, R, x_src, kc, vc, y=y, ws=ws)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(gr, stream=s):
+                for _ in range(n):
+                    E.layer_forward(p, lw, idx, R, x_src, kc, vc, y=y, ws=ws)
+        torch.cuda.current_stream().wait_stream(s)
+        warm_replay(gr, 50.0)
+        us = statistics.median(replay_ms([gr], dev) for _ in range(3)) * 1e3 / n
+        rows = int(R.sum().item())
+        params = d * (d + 2 * w.Hkv * w.D) + d * d + 3 * d * dff
+        wbytes = 2 * params
+        flops = 2 * rows * params + 4 * w.Hq * rows * L * w.D
+        pk = peaks()
+        out[name] = {"R": rows, "us": us, "weight_GB/s": wbytes / (us * 1e3), "TFLOP/s": flops / (us * 1e6),
+                     "frac_hbm": wbytes / (us * 1e3) / pk["hbm_gbs"], "frac_bf16": flops / (us * 1e6) / pk["bf16_tflops"]}
+        del gr
+    out["full_over_partial"] = out["full"]["us"] / out["partial"]["us"]
+    out["workload"] = (f"one LLaDA-8B-shaped layer: d {d}, {w.Hq} x {w.D} MHA, d_ff {dff}, L {L}; RMSNorm, QKV + RoPE, "
+                       f"K/V refresh, attention, O-proj + residual, RMSNorm, SwiGLU, down + residual")
+    out["weights_MB"] = 2 * (d * (d + 2 * w.Hkv * w.D) + d * d + 3 * d * dff) / 1e6
+    del lw, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_configs(E, dev, args) -> dict:
     """Every synthetic workload besides the headline: workload 1 (tiny, fp32 logits), the
     headline layer with tau below every entropy (a full step, R = L), workload 3 (the Dream-7B
@@ -611,6 +680,7 @@ def run_configs(E, dev, args) -> dict:
     out["dream_gqa"] = config_entry(E, W.workload(3), dev, 50, "device", 3)
     out["long_context"] = config_entry(E, W.workload(5), dev, 500, "device", 5)
     out["llada_trace"] = run_trace(E, dev, args.trace_steps)
+    out["llada_layer_forward"] = run_layer_forward(E, dev, 200)
     return out
 
 

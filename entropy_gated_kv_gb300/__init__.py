@@ -38,6 +38,10 @@ __all__ = [
     "partial_attention_workspace_size",
     "step",
     "step_workspace_size",
+    "LayerWeights",
+    "rope_table",
+    "layer_forward",
+    "layer_forward_workspace_size",
     "read_device_error",
     "EcError",
 ]
@@ -256,6 +260,67 @@ def partial_attention(p: Params, q, k_cache, v_cache, R, out, scale: float | Non
                                     _vp(ws), ws.numel(), _vp(dev_err), _stream(stream))
     C.check(st, "ec_partial_attention")
     return out
+
+
+@dataclass
+class LayerWeights:
+    """Weights of one LLaMA-style layer for layer_forward (ec_layer): CUDA bf16 tensors wq
+    [Hq D, d], wk and wv [Hkv D, d], wo [d, Hq D], wg and wu [d_ff, d], wd [d, d_ff], gamma1 and
+    gamma2 [d]; rope_cos and rope_sin fp32 [L, D / 2] (rope_table)."""
+
+    wq: torch.Tensor
+    wk: torch.Tensor
+    wv: torch.Tensor
+    wo: torch.Tensor
+    wg: torch.Tensor
+    wu: torch.Tensor
+    wd: torch.Tensor
+    gamma1: torch.Tensor
+    gamma2: torch.Tensor
+    rope_cos: torch.Tensor
+    rope_sin: torch.Tensor
+    eps: float = 1e-5
+
+    @property
+    def d_ff(self) -> int:
+        return int(self.wg.shape[0])
+
+    def c(self) -> C.EcLayer:
+        return C.EcLayer(self.d_ff, float(self.eps), *[_vp(getattr(self, n)) for n in
+                                                      ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "gamma1", "gamma2",
+                                                       "rope_cos", "rope_sin")])
+
+
+def rope_table(L: int, D: int, theta: float, device="cuda", stream=None):
+    """RoPE cos / sin tables fp32 [L, D / 2] of the angles pos * theta^(-2i / D), built on the
+    device in double precision (ec_rope_table)."""
+    cs = torch.empty(L, D // 2, dtype=torch.float32, device=device)
+    sn = torch.empty(L, D // 2, dtype=torch.float32, device=device)
+    st = lib().ec_rope_table(int(L), int(D), float(theta), _vp(cs), _vp(sn), _stream(stream))
+    C.check(st, "ec_rope_table")
+    return cs, sn
+
+
+def layer_forward_workspace_size(p: Params, d_ff: int) -> int:
+    pc = p.c()
+    return int(lib().ec_layer_forward_workspace_size(ctypes.byref(pc), int(d_ff)))
+
+
+def layer_forward(p: Params, w: LayerWeights, idx, R, x_src, k_cache, v_cache, y=None, ws=None, dev_err=None,
+                  stream=None):
+    """The partial (R < L) or full forward of one layer for the recompute rows idx[b, :R[b]]
+    (ec_layer_forward): refreshes k_cache / v_cache at those positions and returns y [B, L, d]
+    (rows in recompute order, the first R[b] written)."""
+    B, L, d = x_src.shape
+    if y is None:
+        y = torch.empty(B, L, d, dtype=torch.bfloat16, device=x_src.device)
+    if ws is None:
+        ws = workspace(layer_forward_workspace_size(p, w.d_ff), x_src.device)
+    pc, wc = p.c(), w.c()
+    st = lib().ec_layer_forward(ctypes.byref(pc), ctypes.byref(wc), _vp(idx), _vp(R), _vp(x_src), _vp(k_cache),
+                                _vp(v_cache), _vp(y), _vp(ws), ws.numel(), _vp(dev_err), _stream(stream))
+    C.check(st, "ec_layer_forward")
+    return y
 
 
 def step_workspace_size(p: Params) -> int:

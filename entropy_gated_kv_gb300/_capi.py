@@ -51,6 +51,13 @@ class EcState(ctypes.Structure):
     ]
 
 
+class EcLayer(ctypes.Structure):
+    _fields_ = [
+        ("d_ff", _i32), ("eps", _f32), ("wq", _p), ("wk", _p), ("wv", _p), ("wo", _p), ("wg", _p), ("wu", _p),
+        ("wd", _p), ("gamma1", _p), ("gamma2", _p), ("rope_cos", _p), ("rope_sin", _p),
+    ]
+
+
 # name -> (restype, argtypes)
 SIGNATURES: dict[str, tuple] = {
     "ec_status_string": (ctypes.c_char_p, [_i32]),
@@ -61,6 +68,9 @@ SIGNATURES: dict[str, tuple] = {
     "ec_entropy_decode_noalloc": (_i32, [_p, _i64, _i32, _i32, _i32, _p, _p, _p, _p]),
     "ec_selftest_bounded_wait": (_i32, [_p, ctypes.c_uint64, _p]),
     "ec_candidates": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p]),
+    "ec_layer_forward_workspace_size": (_sz, [_p, _i32]),
+    "ec_layer_forward": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
+    "ec_rope_table": (_i32, [_i32, _i32, _f32, _p, _p, _p]),
     "ec_lm_head_entropy_workspace_size": (_sz, [_i32]),
     "ec_lm_head_entropy": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_select_recompute": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _p, _p, _p]),

@@ -290,6 +290,48 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
   return st;
 }
 
+// ---- the partial forward of one layer --------------------------------------------------------------
+namespace {
+ec_status check_layer(const ec_params* p, const ec_layer* w) {
+  ec_status r = check_params(p, kCheckAttn);
+  if (r != EC_OK) return r;
+  if (w == nullptr) return EC_ERR_INVALID_ARG;
+  const int64_t d = static_cast<int64_t>(p->Hq) * p->D, kvf = static_cast<int64_t>(p->Hkv) * p->D;
+  if (d % 128 != 0 || d > 8192 || kvf % 128 != 0) return EC_ERR_UNSUPPORTED;
+  if (w->d_ff < 64 || w->d_ff % 64 != 0 || w->d_ff > 65536) return EC_ERR_INVALID_ARG;
+  if (!(w->eps > 0.f)) return EC_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->wq, w->wk, w->wv, w->wo, w->wg, w->wu, w->wd, w->gamma1, w->gamma2, w->rope_cos, w->rope_sin};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return EC_ERR_INVALID_ARG;
+  return EC_OK;
+}
+}  // namespace
+
+size_t ec_layer_forward_workspace_size(const ec_params* p, int32_t d_ff) {
+  if (check_params(p, kCheckAttn) != EC_OK || d_ff < 64 || d_ff % 64 != 0) return 0;
+  return layer_forward_workspace_bytes(*p, d_ff);
+}
+
+ec_status ec_layer_forward(const ec_params* p, const ec_layer* w, const int32_t* idx, const int32_t* R,
+                           const void* x_src, void* k_cache, void* v_cache, void* y, void* ws, size_t ws_bytes,
+                           int32_t* dev_err, ec_stream_t stream) {
+  ec_status r = check_layer(p, w);
+  if (r != EC_OK) return r;
+  if (!idx || !R || !x_src || !k_cache || !v_cache || !y || !ws) return EC_ERR_INVALID_ARG;
+  if (!aligned16(x_src) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(y) || !aligned16(ws))
+    return EC_ERR_INVALID_ARG;
+  if (ws_bytes < layer_forward_workspace_bytes(*p, w->d_ff)) return EC_ERR_INVALID_ARG;
+  ec_status st = EC_OK;
+  launch_layer_forward(*p, *w, idx, R, x_src, k_cache, v_cache, y, ws, dev_err, static_cast<cudaStream_t>(stream), &st);
+  return st;
+}
+
+ec_status ec_rope_table(int32_t L, int32_t D, float theta, float* rope_cos, float* rope_sin, ec_stream_t stream) {
+  if (L < 1 || L > kMaxL || D < 2 || D > 256 || D % 2 != 0 || !(theta > 0.f)) return EC_ERR_INVALID_ARG;
+  if (!rope_cos || !rope_sin) return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_rope_table(L, D, theta, rope_cos, rope_sin, static_cast<cudaStream_t>(stream)));
+}
+
 // ---- whole step ---------------------------------------------------------------------------------
 size_t ec_step_workspace_size(const ec_params* p) {
   if (check_params(p, kCheckDecode | kCheckSelect | kCheckAttn) != EC_OK) return 0;

@@ -75,6 +75,13 @@ cudaError_t launch_partial_attention(const ec_params& p, const void* q, const vo
                                      const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
                                      int32_t* dev_err, bool plan_early, cudaStream_t s, ec_status* status);
 
+// ---- the partial forward of one layer (layer_forward.cu) ----------------------------------
+size_t layer_forward_workspace_bytes(const ec_params& p, int32_t d_ff);
+cudaError_t launch_layer_forward(const ec_params& p, const ec_layer& w, const int32_t* idx, const int32_t* R,
+                                 const void* x_src, void* k_cache, void* v_cache, void* y, void* ws,
+                                 int32_t* dev_err, cudaStream_t s, ec_status* status);
+cudaError_t launch_rope_table(int32_t L, int32_t D, float theta, float* cs, float* sn, cudaStream_t s);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The gate's scope [lo, hi): the whole sequence unless the caller set one (ec_params).

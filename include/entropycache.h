@@ -18,8 +18,10 @@
  *                                                  -> ec_partial_attention
  *   ec_step runs (a)(b)(c) once and then (c-scatter)(d) for every layer.
  *
- * Beyond the step: ec_lm_head_entropy computes (a) from the candidates' hidden states (the
- * output projection fused with the decode, so the logits are never stored);
+ * Beyond the step: ec_layer_forward runs the partial (or full) forward of one transformer layer
+ * for the recompute set; ec_lm_head_entropy computes (a) from the candidates' hidden states (the
+ * output projection fused with the decode, so the logits are never stored); ec_candidates builds
+ * a step's candidates for block-wise or sliding-window decoding;
  * ec_entropy_decode_noalloc is (a) for callers that cannot allocate a workspace; and
  * ec_selftest_bounded_wait exercises the kernels' timeout path.
  *
@@ -313,6 +315,49 @@ size_t ec_partial_attention_workspace_size(const ec_params* p);
 ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* R, float scale, void* out,
                                void* ws, size_t ws_bytes, int32_t* dev_err, ec_stream_t stream);
+
+/* ---- the partial forward of one transformer layer ------------------------------------------
+ * The forward pass the step's flag selects (EntropyCache, gist.science zh summary §2.2,
+ * "前向传播 / 部分传播"): a partial forward recomputes only the recompute set (idx, R as
+ * built by ec_select_recompute) and reads every other position from the K/V cache; with the
+ * full set (R = L) it is the full forward. The layer is the LLaMA-style block of the models the
+ * pages evaluate (LLaDA-8B, Dream-7B; the pages name the models, not their layers). For each
+ * sequence b and recompute row r < R[b] at position p = idx[b, r]:
+ *   x = x_src[b, p];  h = RMSNorm(x) * gamma1           (x / sqrt(mean(x^2) + eps))
+ *   q = h wq^T, k = h wk^T, v = h wv^T; q and k rotated by RoPE at position p (rotate-half:
+ *       feature i and i + D/2 of a head turn by the angle p * theta^(-2i/D), from rope_cos /
+ *       rope_sin, see ec_rope_table)
+ *   k_cache[b, p] = k, v_cache[b, p] = v                 (the K/V refresh of the recompute set)
+ *   o = attention of q against the whole cache (as ec_partial_attention, scale 1/sqrt(D); with
+ *       a gate scope, the keys [0, scope_hi))
+ *   x2 = x + o wo^T;  h2 = RMSNorm(x2) * gamma2;  y[b, r] = x2 + (SiLU(h2 wg^T) * (h2 wu^T)) wd^T
+ * Shapes (params p: B, L, Hq, Hkv, D; d = Hq * D is the model width):
+ *   wq [Hq D, d], wk and wv [Hkv D, d], wo [d, Hq D], wg and wu [d_ff, d], wd [d, d_ff],
+ *   gamma1 and gamma2 [d]: bf16, row-major (out, in), 16-byte aligned;
+ *   rope_cos, rope_sin fp32 [L, D / 2];  x_src bf16 [B, L, d] (position-indexed layer input);
+ *   k_cache, v_cache bf16 [B, L, Hkv, D];  y bf16 [B, L, d] (rows in recompute order, the
+ *   first R[b] written);  idx int32 [B, L], R int32 [B] on the device (no host synchronisation).
+ * d % 128 == 0, d <= 8192, (Hkv D) % 128 == 0, d_ff % 64 == 0; eps > 0.
+ * Products on bf16 tensor cores with fp32 accumulation; every intermediate (h, q, k, v, o, x2,
+ * h2, the SwiGLU output) is rounded to bf16. ws: ec_layer_forward_workspace_size(p, d_ff)
+ * bytes, no initial contents needed. */
+typedef struct ec_layer {
+  int32_t d_ff;
+  float eps;
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+  const void *gamma1, *gamma2;
+  const float *rope_cos, *rope_sin;
+} ec_layer;
+
+size_t ec_layer_forward_workspace_size(const ec_params* p, int32_t d_ff);
+ec_status ec_layer_forward(const ec_params* p, const ec_layer* w, const int32_t* idx, const int32_t* R,
+                           const void* x_src, void* k_cache, void* v_cache, void* y, void* ws, size_t ws_bytes,
+                           int32_t* dev_err, ec_stream_t stream);
+
+/* The RoPE table of ec_layer_forward: cos and sin of pos * theta^(-2i / D) for pos < L and
+ * i < D / 2, computed on the device in double precision and stored as fp32 [L, D / 2].
+ * 1 <= L, D even (2 .. 256), theta > 0. */
+ec_status ec_rope_table(int32_t L, int32_t D, float theta, float* rope_cos, float* rope_sin, ec_stream_t stream);
 
 /* ---- one whole denoising step ---------------------------------------------------------------
  * Runs the three stages of the workflow in order (zh summary §2.2): (a) decode and

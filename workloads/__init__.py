@@ -49,6 +49,8 @@ __all__ = [
     "layer_pool",
     "layer_tensors",
     "trace_candidates",
+    "layer_weights",
+    "layer_input",
 ]
 
 
@@ -306,3 +308,30 @@ def lm_head_inputs(n_rows: int, d_model: int, V: int, seed: int = 0, peaked: int
         wv = bf16_bits_to_f32(weight[v]).astype(np.float64)
         hidden[i] += (12.0 + i) * wv / max(float(wv @ wv), 1e-30)
     return to_bf16_bits(hidden), weight
+
+
+def layer_weights(d: int, Hq: int, Hkv: int, D: int, d_ff: int, seed: int = 0) -> dict:
+    """One LLaMA-style layer's weights as bf16 bit patterns, at the usual initialisation scale
+    (activations stay about unit size): wq [Hq D, d], wk, wv [Hkv D, d], wo [d, Hq D] and wg, wu
+    [d_ff, d] ~ N(0, 1 / fan_in); wd [d, d_ff] ~ N(0, 1 / d_ff); gamma1, gamma2 [d] ~ 1 + N(0,
+    0.1^2). Drawn in float32 chunks of rows."""
+    r = rng_for(seed, 60)
+
+    def mat(rows: int, cols: int) -> np.ndarray:
+        out = np.empty((rows, cols), dtype=np.uint16)
+        for a in range(0, rows, 2048):
+            b = min(rows, a + 2048)
+            out[a:b] = to_bf16_bits(r.standard_normal((b - a, cols), dtype=np.float32) / np.float32(np.sqrt(cols)))
+        return out
+
+    return {
+        "wq": mat(Hq * D, d), "wk": mat(Hkv * D, d), "wv": mat(Hkv * D, d), "wo": mat(d, Hq * D),
+        "wg": mat(d_ff, d), "wu": mat(d_ff, d), "wd": mat(d, d_ff),
+        "gamma1": to_bf16_bits(1.0 + 0.1 * r.standard_normal(d, dtype=np.float32)),
+        "gamma2": to_bf16_bits(1.0 + 0.1 * r.standard_normal(d, dtype=np.float32)),
+    }
+
+
+def layer_input(B: int, L: int, d: int, seed: int = 0) -> np.ndarray:
+    """The layer input at every position, bf16 bits [B, L, d] ~ N(0, 1)."""
+    return _normal_bf16(rng_for(seed, 61), (B, L, d))

@@ -16,7 +16,9 @@
 //   - gemm_kernel<EPI>: a swap-AB tcgen05 GEMM, out[row, f] = sum_k X[row, k] W[f, k]. M = 128
 //     weight rows (output features, A, K-major), N = the block's recompute rows rounded up to
 //     32 (B, K-major, at most 256; the instruction descriptor is built on the device from R),
-//     K in stages of 64 (one 128-byte swizzle atom per row) through a 4-stage TMA ring. One
+//     K in stages of 64 (one 128-byte swizzle atom per row) through a TMA ring of up to 8
+//     stages (as many as fit beside the row blocks' rows: more weight bytes in flight when the
+//     rows are few), the row operand in boxes of 128 rows. One
 //     thread issues tcgen05.mma into a double-buffered TMEM accumulator (2 x 256 columns), so a
 //     tile's epilogue overlaps the next tile's products. Persistent, one CTA per SM; the tiles
 //     are (feature tile, live row block) with the feature tile outermost, so that the row
@@ -44,11 +46,12 @@ constexpr int kTileM = 128;     // output features per tile (MMA M)
 constexpr int kTileK = 64;      // input features per stage (one 128-byte swizzle atom)
 constexpr int kRowBlock = 256;  // recompute rows per tile (MMA N at most)
 constexpr int kBoxRows = 128;   // rows per TMA box of the row operand
-constexpr int kStages = 4;
-constexpr uint32_t kABytes = kTileM * kTileK * 2;     // 16 KB
+constexpr int kMaxStages = 8;
+constexpr uint32_t kABytes = kTileM * kTileK * 2;      // 16 KB
 constexpr uint32_t kBoxBytes = kBoxRows * kTileK * 2;  // 16 KB
-constexpr uint32_t kBBytes = kRowBlock * kTileK * 2;   // 32 KB
+constexpr uint32_t kRingBytes = 196 * 1024;            // A and B stages
 constexpr int kXPitch = 129;                           // exchange buffer row pitch (floats)
+constexpr int kMaxGrid = 256;                          // GEMM CTAs at most (the split-K slab is sized by it)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s: far beyond any legitimate wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kDescHi = sdesc_hi(1024);  // 8 rows of 128 B between core-matrix groups
@@ -56,8 +59,8 @@ constexpr uint32_t kDescHi = sdesc_hi(1024);  // 8 rows of 128 B between core-ma
 enum : int { kEpiQkv = 0, kEpiResidual = 1, kEpiSwiglu = 2 };
 
 struct GemmBars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
@@ -65,9 +68,7 @@ struct GemmBars {
   int epi_ok;  // the epilogue's shared verdict on its latest wait
 };
 
-constexpr uint32_t kAOff = 0;
-constexpr uint32_t kBOff = kStages * kABytes;
-constexpr uint32_t kXOff = kBOff + kStages * kBBytes;
+constexpr uint32_t kXOff = kRingBytes;
 constexpr uint32_t kBarOff = kXOff + 32 * kXPitch * 4;
 constexpr uint32_t kSmemBytes = kBarOff + sizeof(GemmBars) + 1024;  // + slack for 1024-byte alignment
 
@@ -84,6 +85,8 @@ struct GemmArgs {
   int q_feats, kv_feats, D;
   const float* rope_cos;  // [L, D/2]
   const float* rope_sin;
+  float* slab;    // split-K partials: [grid][kRowBlock][kTileM] fp32
+  int grid;       // the GEMM's grid (the finishing kernel recomputes the plan from it)
   int32_t* dev_err;
 };
 
@@ -98,7 +101,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
 // Live row blocks: sequence b has ceil(R[b] / 256) of them. Tiles are (feature tile, live row
 // block), the feature tile outermost, so that the row blocks of one weight tile run together.
 __device__ __forceinline__ int live_blocks(const GemmArgs& a, int b) {
-  const int Rb = min(max(__ldcg(a.R + b), 0), a.L);
+  const int Rb = min(max(__ldg(a.R + b), 0), a.L);  // R is read-only while the kernel runs
   return (Rb + kRowBlock - 1) / kRowBlock;
 }
 
@@ -118,7 +121,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_rb, const GemmArgs&
     ++x.b;
   }
   x.r0 = j * kRowBlock;
-  const int Rb = min(max(__ldcg(a.R + x.b), 0), a.L);
+  const int Rb = min(max(__ldg(a.R + x.b), 0), a.L);
   x.nrows = min(kRowBlock, Rb - x.r0);
   return x;
 }
@@ -128,6 +131,106 @@ __device__ __forceinline__ float silu(float g) { return g / (1.f + ex2_approx(-g
 __device__ __forceinline__ uint16_t to_bf16(float v) { return static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
 
 __device__ __forceinline__ float from_bf16(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
+
+// Split-K plan, the same in every CTA of the GEMM and of its finishing kernel: when there are
+// fewer live tiles than CTAs, each tile's K stages are split over up to kMaxSplits CTAs, which
+// write fp32 partials to the slab; the finishing kernel sums them and runs the epilogue.
+constexpr int kMaxSplits = 4;
+
+struct SplitPlan {
+  int total_rb, live, splits, kps;  // live row blocks, live tiles, splits per tile, K stages per split
+  int n_max;                        // rows of the largest row block, rounded up to 32
+};
+
+__device__ __forceinline__ SplitPlan split_plan(const GemmArgs& a) {
+  SplitPlan sp;
+  sp.total_rb = 0;
+  int rmax = 0;
+  for (int b = 0; b < a.B; ++b) {
+    const int Rb = min(max(__ldg(a.R + b), 0), a.L);
+    sp.total_rb += (Rb + kRowBlock - 1) / kRowBlock;
+    rmax = max(rmax, Rb);
+  }
+  sp.n_max = min(kRowBlock, (rmax + 31) / 32 * 32);
+  sp.live = a.n_ftiles * sp.total_rb;
+  const int n_k = a.K / kTileK;
+  // up to two work units per CTA when the row blocks are small (the slab then holds at most
+  // 2 grid blocks of 128 rows), otherwise one
+  const int units = sp.n_max <= kRowBlock / 2 ? 2 * a.grid : a.grid;
+  int s = sp.live > 0 ? max(1, min(kMaxSplits, units / sp.live)) : 1;
+  s = min(s, n_k);
+  sp.kps = (n_k + s - 1) / s;
+  sp.splits = (n_k + sp.kps - 1) / sp.kps;  // no empty split
+  return sp;
+}
+
+// A work unit's block of the slab: n_max rows of 128 fp32 features (the slab holds grid x 256
+// rows, so 2 grid units of at most 128 rows or grid units of 256).
+__device__ __forceinline__ float* slab_block(const GemmArgs& a, const SplitPlan& sp, int tile_id, int split) {
+  return a.slab + static_cast<int64_t>(tile_id * sp.splits + split) * sp.n_max * kTileM;
+}
+
+// The fused epilogue of 32 rows (chunk ch of tile x) of one output feature per thread: v[c] is
+// the accumulator of row 32 ch + c. All 128 threads of the epilogue call it; bar() synchronises
+// them (the exchange buffer sX carries the RoPE partner or the SwiGLU up value).
+template <int EPI, typename Bar>
+__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x, int ch, const float (&v)[32],
+                                               float* sX, int f_in, Bar bar) {
+  const int nvalid = min(32, x.nrows - ch * 32);
+  const int64_t rbase = static_cast<int64_t>(x.b) * a.L + x.r0 + ch * 32;
+  if constexpr (EPI == kEpiResidual) {
+    const int f = x.ft * kTileM + f_in;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (c < nvalid) {
+        const int64_t o = (rbase + c) * a.n_out + f;
+        a.out0[o] = to_bf16(v[c] + from_bf16(a.res[o]));
+      }
+    }
+  } else if constexpr (EPI == kEpiSwiglu) {
+    bar();  // the exchange buffer is free
+    if (f_in >= 64)
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = v[c];
+    bar();
+    if (f_in < 64) {
+      const int f = x.ft * 64 + f_in;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) a.out0[(rbase + c) * a.n_out + f] = to_bf16(silu(v[c]) * sX[c * kXPitch + f_in + 64]);
+    }
+  } else {  // q / k with RoPE, v as is
+    const int f0 = x.ft * kTileM;
+    const int part = f0 < a.q_feats ? 0 : (f0 < a.q_feats + a.kv_feats ? 1 : 2);
+    uint16_t* dst = part == 0 ? a.out0 : (part == 1 ? a.out1 : a.out2);
+    const int feats = part == 0 ? a.q_feats : a.kv_feats;
+    const int f = f0 - (part == 0 ? 0 : (part == 1 ? a.q_feats : a.q_feats + a.kv_feats)) + f_in;
+    if (part == 2) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nvalid) dst[(rbase + c) * feats + f] = to_bf16(v[c]);
+    } else {
+      const int half = a.D / 2;
+      const int j = f_in % a.D;  // feature within its head (a tile holds whole heads)
+      const int i = j % half;
+      bar();  // the exchange buffer is free
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = v[c];
+      bar();
+      const int partner = f_in ^ half;  // the rotate-half partner in the same head
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (c < nvalid) {
+          const int pos = min(max(__ldg(a.idx + rbase + c), 0), a.L - 1);  // a bad idx is reported by the norm
+          const float cs = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
+          const float sn = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
+          const float w = sX[c * kXPitch + partner];
+          dst[(rbase + c) * feats + f] = to_bf16(j < half ? v[c] * cs - w * sn : v[c] * cs + w * sn);
+        }
+      }
+    }
+  }
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
@@ -140,9 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   float* sX = reinterpret_cast<float*>(smem + kXOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_k = a.K / kTileK;
+  (void)n_k;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&bars->full[i], 1);
       mbar_init(&bars->empty[i], 1);
     }
@@ -170,9 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   volatile int* abort_flag = &bars->abort;
   pdl_wait();  // the row operand, R and idx come from the previous kernels in the stream
   pdl_launch_dependents();
-  int total_rb = 0;
-  for (int b = 0; b < a.B; ++b) total_rb += live_blocks(a, b);
-  const int n_tiles = a.n_ftiles * total_rb;
+  const SplitPlan sp = split_plan(a);
+  const int n_tiles = sp.live * sp.splits;
+  // the ring: as many stages as fit for the launch's largest row block (more weight bytes in
+  // flight when the rows are few)
+  const uint32_t b_bytes = static_cast<uint32_t>((sp.n_max + kBoxRows - 1) / kBoxRows) * kBoxBytes;
+  const int stages = max(2, min(kMaxStages, static_cast<int>(kRingBytes / (kABytes + max(b_bytes, kBoxBytes)))));
+  const uint32_t a_off = 0, b_off = static_cast<uint32_t>(stages) * kABytes;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -180,14 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const Tile x = decode_tile(t, total_rb, a);
+        const Tile x = decode_tile(t / sp.splits, sp.total_rb, a);
+        const int k0 = (t % sp.splits) * sp.kps, k1 = min(n_k, k0 + sp.kps);
         const int nbox = (x.nrows + kBoxRows - 1) / kBoxRows;
         const int xrow = x.b * a.L + x.r0;
-        for (int kt = 0; kt < n_k; ++kt, ++it) {
-          const uint32_t s = it % kStages, u = it / kStages;
+        for (int kt = k0; kt < k1; ++kt, ++it) {
+          const uint32_t s = it % stages, u = it / stages;
           if (!(ok = mbar_wait_bounded(&bars->empty[s], (u & 1u) ^ 1u, abort_flag, a.dev_err, kWaitLimitNs))) break;
           mbar_arrive_expect_tx(&bars->full[s], kABytes + nbox * kBoxBytes);
-          uint8_t* as = smem + kAOff + s * kABytes;
+          uint8_t* as = smem + a_off + s * kABytes;
           if constexpr (EPI == kEpiQkv) {
             const int f0 = x.ft * kTileM;
             if (f0 < a.q_feats) tma_load_2d(as, &tm_a0, &bars->full[s], kt * kTileK, f0);
@@ -200,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tma_load_2d(as, &tm_a0, &bars->full[s], kt * kTileK, x.ft * kTileM);
           }
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(smem + kBOff + s * kBBytes + bx * kBoxBytes, &tm_x, &bars->full[s], kt * kTileK,
+            tma_load_2d(smem + b_off + s * b_bytes + bx * kBoxBytes, &tm_x, &bars->full[s], kt * kTileK,
                         xrow + bx * kBoxRows);
         }
       }
@@ -212,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       bool ok = true;
       int n = 0;
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
-        const Tile x = decode_tile(t, total_rb, a);
+        const Tile x = decode_tile(t / sp.splits, sp.total_rb, a);
+        const int k0 = (t % sp.splits) * sp.kps, k1 = min(n_k, k0 + sp.kps);
         const int buf = n & 1;
         const uint32_t use = static_cast<uint32_t>(n >> 1);
         ++n;
@@ -221,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!(ok = mbar_wait_bounded(&bars->acc_empty[buf], (use & 1u) ^ 1u, abort_flag, a.dev_err, kWaitLimitNs))) break;
         tc_fence_after();
         const uint32_t d_col = tmem + static_cast<uint32_t>(buf * kRowBlock);
-        for (int kt = 0; kt < n_k; ++kt, ++it) {
-          const uint32_t s = it % kStages, u = it / kStages;
+        for (int kt = k0; kt < k1; ++kt, ++it) {
+          const uint32_t s = it % stages, u = it / stages;
           if (!(ok = mbar_wait_bounded(&bars->full[s], u & 1u, abort_flag, a.dev_err, kWaitLimitNs))) break;
           tc_fence_after();
-          const uint32_t a_lo = sdesc_lo(smem_u32(smem + kAOff + s * kABytes), 16);
-          const uint32_t b_lo = sdesc_lo(smem_u32(smem + kBOff + s * kBBytes), 16);
+          const uint32_t a_lo = sdesc_lo(smem_u32(smem + a_off + s * kABytes), 16);
+          const uint32_t b_lo = sdesc_lo(smem_u32(smem + b_off + s * b_bytes), 16);
 #pragma unroll
           for (int kk = 0; kk < kTileK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
-            umma_ss(d_col, a_lo + 2 * kk, b_lo + 2 * kk, kDescHi, idesc, (kt > 0 || kk > 0) ? 1u : 0u);
+            umma_ss(d_col, a_lo + 2 * kk, b_lo + 2 * kk, kDescHi, idesc, (kt > k0 || kk > 0) ? 1u : 0u);
           umma_commit(&bars->empty[s]);
         }
         if (ok) umma_commit(&bars->acc_full[buf]);
@@ -242,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int f_in = 32 * (warp & 3) + lane;  // (tcgen05 warp rule: warp w reads lanes 32 (w % 4) ..)
     int n = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const Tile x = decode_tile(t, total_rb, a);
+      const int tile_id = t / sp.splits, split = t % sp.splits;
+      const Tile x = decode_tile(tile_id, sp.total_rb, a);
       const int buf = n & 1;
       const uint32_t use = static_cast<uint32_t>(n >> 1);
       ++n;
@@ -254,7 +365,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       named_bar_sync(1, 128);
       if (!bars->epi_ok) break;
       tc_fence_after();
-      const int64_t row0 = static_cast<int64_t>(x.b) * a.L + x.r0;
       for (int ch = 0; ch < n_chunks; ++ch) {
         uint32_t r[32];
         EC_TMEM_LD32(tmem + lane_off + static_cast<uint32_t>(buf * kRowBlock + ch * 32), r);
@@ -263,63 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tc_fence_before();
           mbar_arrive(&bars->acc_empty[buf]);
         }
-        const int nvalid = min(32, x.nrows - ch * 32);
-        const int64_t rbase = row0 + ch * 32;
-        if constexpr (EPI == kEpiResidual) {
-          const int f = x.ft * kTileM + f_in;
+        float v[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c < nvalid) {
-              const int64_t o = (rbase + c) * a.n_out + f;
-              a.out0[o] = to_bf16(__uint_as_float(r[c]) + from_bf16(a.res[o]));
-            }
-          }
-        } else if constexpr (EPI == kEpiSwiglu) {
-          named_bar_sync(1, 128);  // the exchange buffer is free
-          if (f_in >= 64)
+        for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
+        if (sp.splits == 1) {
+          epilogue_chunk<EPI>(a, x, ch, v, sX, f_in, [] { named_bar_sync(1, 128); });
+        } else {  // a split's partial: rows of 128 fp32 features, coalesced
+          float* blk = slab_block(a, sp, tile_id, split) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = __uint_as_float(r[c]);
-          named_bar_sync(1, 128);
-          if (f_in < 64) {
-            const int f = x.ft * 64 + f_in;
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (c < nvalid) {
-                const float g = __uint_as_float(r[c]), u = sX[c * kXPitch + f_in + 64];
-                a.out0[(rbase + c) * a.n_out + f] = to_bf16(silu(g) * u);
-              }
-            }
-          }
-        } else {  // q / k with RoPE, v as is
-          const int f0 = x.ft * kTileM;
-          const int part = f0 < a.q_feats ? 0 : (f0 < a.q_feats + a.kv_feats ? 1 : 2);
-          uint16_t* dst = part == 0 ? a.out0 : (part == 1 ? a.out1 : a.out2);
-          const int feats = part == 0 ? a.q_feats : a.kv_feats;
-          const int f = f0 - (part == 0 ? 0 : (part == 1 ? a.q_feats : a.q_feats + a.kv_feats)) + f_in;
-          if (part == 2) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c < nvalid) dst[(rbase + c) * feats + f] = to_bf16(__uint_as_float(r[c]));
-          } else {
-            const int half = a.D / 2;
-            const int j = f_in % a.D;  // feature within its head (a tile holds whole heads)
-            const int i = j % half;
-            named_bar_sync(1, 128);  // the exchange buffer is free
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = __uint_as_float(r[c]);
-            named_bar_sync(1, 128);
-            const int partner = f_in ^ half;  // the rotate-half partner in the same head
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              if (c < nvalid) {
-                const int pos = min(max(__ldg(a.idx + rbase + c), 0), a.L - 1);  // a bad idx is reported by the norm
-                const float cs = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
-                const float sn = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
-                const float v = __uint_as_float(r[c]), w = sX[c * kXPitch + partner];
-                dst[(rbase + c) * feats + f] = to_bf16(j < half ? v * cs - w * sn : v * cs + w * sn);
-              }
-            }
-          }
+          for (int c = 0; c < 32; ++c) blk[c * kTileM] = v[c];
         }
       }
     }
@@ -331,6 +393,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Sums the split-K partials of each (tile, 32-row chunk) and runs the fused epilogue; nothing
+// when the GEMM ran unsplit. 128 threads, one output feature each.
+template <int EPI>
+__global__ void __launch_bounds__(128) gemm_finish_kernel(GemmArgs a) {
+  __shared__ float sX[32 * kXPitch];
+  pdl_wait();  // the partials come from the GEMM
+  pdl_launch_dependents();
+  const SplitPlan sp = split_plan(a);
+  if (sp.splits == 1) return;
+  const int f_in = threadIdx.x;
+  const int items = sp.live * (kRowBlock / 32);
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {  // uniform over the CTA
+    const int tile_id = it / (kRowBlock / 32), ch = it - tile_id * (kRowBlock / 32);
+    const Tile x = decode_tile(tile_id, sp.total_rb, a);
+    if (ch * 32 >= x.nrows) continue;
+    float v[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) v[c] = 0.f;
+    float t[kMaxSplits][32];  // every split's values in flight at once before any is added
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+      if (s < sp.splits) {
+        const float* blk = slab_block(a, sp, tile_id, s) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) t[s][c] = blk[c * kTileM];
+      }
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < sp.splits)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] += t[s][c];
+    epilogue_chunk<EPI>(a, x, ch, v, sX, f_in, [] { __syncthreads(); });
   }
 }
 
@@ -452,9 +550,11 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   int sms = 0;
   if (e == cudaSuccess) e = current_device_sms(&sms);
   if (e != cudaSuccess) return e;
-  const int n_tiles = args.n_ftiles * args.B * args.nrb;  // at most: rows beyond R[b] make no tile
-  const int grid = std::max(1, std::min(sms, n_tiles));
-  return launch_pdl(gemm_kernel<EPI>, dim3(grid), dim3(kThreads), kSmemBytes, s, a0, a1, a2, x, args);
+  GemmArgs g = args;
+  g.grid = std::max(1, std::min(sms, kMaxGrid));
+  e = launch_pdl(gemm_kernel<EPI>, dim3(g.grid), dim3(kThreads), kSmemBytes, s, a0, a1, a2, x, g);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(gemm_finish_kernel<EPI>, dim3(4 * g.grid), dim3(128), 0, s, g);
 }
 
 }  // namespace
@@ -465,6 +565,7 @@ size_t layer_forward_workspace_bytes(const ec_params& p, int32_t d_ff) {
   const size_t kv = static_cast<size_t>(p.Hkv) * p.D;
   size_t off = 0;
   for (size_t n : {d, d, d, kv, kv, d, d, static_cast<size_t>(d_ff)}) off += align_up(rows * n * 2, 256);
+  off += align_up(static_cast<size_t>(kMaxGrid) * kRowBlock * kTileM * 4, 256);  // split-K partials
   return off + align_up(attention_workspace_bytes(p), 256);
 }
 
@@ -503,6 +604,8 @@ cudaError_t launch_layer_forward(const ec_params& p, const ec_layer& w, const in
   uint16_t* o = take(d);
   uint16_t* x2 = take(d);
   uint16_t* act = take(dff);
+  float* slab = reinterpret_cast<float*>(base + off);
+  off += align_up(static_cast<size_t>(kMaxGrid) * kRowBlock * kTileM * 4, 256);
   void* attn_ws = base + off;
 
   CUtensorMap m_wq, m_wk, m_wv, m_wo, m_wg, m_wu, m_wd, m_h, m_o, m_act;
@@ -534,6 +637,7 @@ cudaError_t launch_layer_forward(const ec_params& p, const ec_layer& w, const in
   ga.D = D;
   ga.rope_cos = w.rope_cos;
   ga.rope_sin = w.rope_sin;
+  ga.slab = slab;
   ga.dev_err = dev_err;
 
   // 1. gather the recompute rows and normalise

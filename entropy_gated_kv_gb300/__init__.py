@@ -352,6 +352,13 @@ def step(p: Params, state: DecodeState, logits, cand_pos, cand_count, layers: li
     C.check(st, "ec_step")
 
 
+def read_floor(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """A plain read of the whole buffer in the decode's launch shape (ec_read_floor): the floor
+    for the decode's read of the same bytes. A measurement aid."""
+    st = lib().ec_read_floor(_vp(buf), buf.numel() * buf.element_size(), _vp(sink), _stream(stream))
+    C.check(st, "ec_read_floor")
+
+
 def selftest_bounded_wait(dev_err: torch.Tensor, limit_ns: int, stream=None) -> None:
     """Runs the library's bounded wait on a barrier nothing completes; afterwards dev_err
     holds EC_DEVERR_TIMEOUT (read it with read_device_error)."""

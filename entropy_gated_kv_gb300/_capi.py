@@ -71,6 +71,7 @@ SIGNATURES: dict[str, tuple] = {
     "ec_layer_forward_workspace_size": (_sz, [_p, _i32]),
     "ec_layer_forward": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
     "ec_rope_table": (_i32, [_i32, _i32, _f32, _p, _p, _p]),
+    "ec_read_floor": (_i32, [_p, _sz, _p, _p]),
     "ec_lm_head_entropy_workspace_size": (_sz, [_i32]),
     "ec_lm_head_entropy": (_i32, [_p, _p, _i32, _i32, _i32, _p, _p, _p, _p, _sz, _p]),
     "ec_select_recompute": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _p, _p, _p]),

@@ -332,6 +332,13 @@ ec_status ec_rope_table(int32_t L, int32_t D, float theta, float* rope_cos, floa
   return cuda_status(launch_rope_table(L, D, theta, rope_cos, rope_sin, static_cast<cudaStream_t>(stream)));
 }
 
+// ---- measurement aid -----------------------------------------------------------------------------
+ec_status ec_read_floor(const void* buf, size_t bytes, uint32_t* sink, ec_stream_t stream) {
+  if (buf == nullptr || sink == nullptr || !aligned16(buf) || bytes % 16 != 0 || bytes > (size_t(1) << 40))
+    return EC_ERR_INVALID_ARG;
+  return cuda_status(launch_read_floor(buf, bytes, sink, static_cast<cudaStream_t>(stream)));
+}
+
 // ---- whole step ---------------------------------------------------------------------------------
 size_t ec_step_workspace_size(const ec_params* p) {
   if (check_params(p, kCheckDecode | kCheckSelect | kCheckAttn) != EC_OK) return 0;

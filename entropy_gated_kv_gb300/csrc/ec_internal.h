@@ -82,6 +82,9 @@ cudaError_t launch_layer_forward(const ec_params& p, const ec_layer& w, const in
                                  int32_t* dev_err, cudaStream_t s, ec_status* status);
 cudaError_t launch_rope_table(int32_t L, int32_t D, float theta, float* cs, float* sn, cudaStream_t s);
 
+// ---- measurement aid (read_floor.cu) ---------------------------------------------------------
+cudaError_t launch_read_floor(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // The gate's scope [lo, hi): the whole sequence unless the caller set one (ec_params).

@@ -163,6 +163,14 @@ ec_status ec_read_device_error(const int32_t* dev_err, int32_t* host_word, ec_st
  * EC_ERR_INVALID_ARG for a NULL dev_err or a limit out of range. */
 ec_status ec_selftest_bounded_wait(int32_t* dev_err, uint64_t limit_ns, ec_stream_t stream);
 
+/* A measurement aid with no counterpart in the pages: reads `bytes` bytes of the device buffer
+ * `buf` in the launch shape of the entropy decode's split launch (one 256-thread CTA per 16 KB,
+ * four 16-byte streaming loads per thread, all in flight at once) and nothing else, so that its
+ * time is the floor for the decode's read of the same bytes. sink: one device word, written
+ * only in the practically impossible case that the folded words equal a fixed constant (it
+ * keeps the loads). buf 16-byte aligned, bytes a multiple of 16. */
+ec_status ec_read_floor(const void* buf, size_t bytes, uint32_t* sink, ec_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t ec_version(void);
 

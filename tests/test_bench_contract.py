@@ -18,10 +18,13 @@ def _args(**kw):
 def _res(ms=25.0, attn_us=9.0, ent_us=6.0):
     return {
         "ms": ms,
-        "kernels": {"R": 95, "entropy_decode_us": ent_us, "partial_attention_us": attn_us, "kv_scatter_us": 2.0},
+        "kernels": {"R": 95, "entropy_decode_us": ent_us, "partial_attention_us": attn_us, "kv_scatter_us": 2.0,
+                    "read_floor_us": 2.7},
         "flag": False,
         "R": 95,
         "copy_mb": 58.0,
+        "ncopy": 17,
+        "touched_mb": 25.0,
         "e2e": {"value": 5000.0, "unit": "steps/s", "h2d_bytes_per_step": 1, "d2h_bytes_per_step": 2},
         "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []},
     }
@@ -128,11 +131,12 @@ def test_config_entry_against_its_binding_roofline():
     import workloads as W
 
     pk = bench.peaks()
-    kern = {"entropy_decode_us": 8.0, "partial_attention_us": 20.0, "kv_scatter_us": 3.0}
+    kern = {"entropy_decode_us": 8.0, "partial_attention_us": 20.0, "kv_scatter_us": 3.0, "read_floor_us": 4.0}
     w = W.workload(2)
     e = bench.summarise_config(w, 20000.0, 1, 1024, kern, 50e6, "host")  # a full step, R = L
     alg = bench.algorithmic(w, 1024)
     assert e["us_per_step"] == pytest.approx(50.0)
+    assert e["entropy_decode"]["of_read_floor"] == pytest.approx(0.5)  # the floor's time over the decode's
     assert e["entropy_decode"]["GB/s"] == pytest.approx(alg["entropy_decode_bytes"] / 8e-6 / 1e9)
     att = e["partial_attention"]
     assert att["bound"] == "tensor"  # 512 flops per byte

@@ -239,3 +239,13 @@ def test_candidates_validation(capi):
     assert lib.ec_candidates(ctypes.byref(p), ctypes.byref(st), 0, 0, 32, None, buf, None) == INV
     bad = _params(capi, scope_lo=3, scope_hi=2)
     assert lib.ec_candidates(ctypes.byref(bad), ctypes.byref(st), 0, 0, 32, buf, buf, None) == INV
+
+
+def test_read_floor_validation(capi):
+    lib = capi.load()
+    INV = capi.EC_ERR_INVALID_ARG
+    buf = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    assert lib.ec_read_floor(None, 1024, buf, None) == INV
+    assert lib.ec_read_floor(buf, 1024, None, None) == INV
+    assert lib.ec_read_floor(ctypes.c_void_p((1 << 20) + 8), 1024, buf, None) == INV  # misaligned
+    assert lib.ec_read_floor(buf, 1000, buf, None) == INV  # not a multiple of 16 bytes

@@ -44,3 +44,16 @@ def test_bounded_wait_times_out_and_the_context_survives(E):
     ids_o, ent_o, conf_o = O.entropy_decode(x.astype(np.float64))
     np.testing.assert_array_equal(ids, ids_o)
     assert np.max(np.abs(ent - ent_o)) <= 1e-3
+
+
+def test_read_floor_reads_without_side_effects():
+    # the measurement aid reads the buffer and leaves the sink alone (it keeps the loads only)
+    import torch
+
+    import entropy_gated_kv_gb300 as E
+
+    buf = torch.arange(3 * 4096 + 8, dtype=torch.int32, device="cuda")  # ragged: not a whole number of CTAs
+    sink = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    E.read_floor(buf, sink)
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 7

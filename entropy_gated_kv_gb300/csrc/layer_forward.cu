@@ -85,7 +85,7 @@ struct GemmArgs {
   int q_feats, kv_feats, D;
   const float* rope_cos;  // [L, D/2]
   const float* rope_sin;
-  float* slab;    // split-K partials: [grid][kRowBlock][kTileM] fp32
+  float* slab;    // split-K partials: kMaxGrid x kRowBlock rows of kTileM fp32, in blocks of n_max rows
   int grid;       // the GEMM's grid (the finishing kernel recomputes the plan from it)
   int32_t* dev_err;
 };
@@ -132,16 +132,21 @@ __device__ __forceinline__ uint16_t to_bf16(float v) { return static_cast<uint16
 
 __device__ __forceinline__ float from_bf16(uint16_t u) { return __uint_as_float(static_cast<uint32_t>(u) << 16); }
 
-// Split-K plan, the same in every CTA of the GEMM and of its finishing kernel: when there are
-// fewer live tiles than CTAs, each tile's K stages are split over up to kMaxSplits CTAs, which
-// write fp32 partials to the slab; the finishing kernel sums them and runs the epilogue.
-constexpr int kMaxSplits = 4;
-
+// Split-K plan, the same in every CTA of the GEMM and of its finishing kernel. A work unit is
+// one split of one live tile (kps K stages); CTA c takes the units c, c + grid, ... Each lane
+// of the warp prices one split count s = lane + 1 as (rounds of units over the grid) x (K stages
+// per unit + 1 for the unit's start-up) and the warp takes the cheapest, the fewer splits on a
+// tie: the split evens out the last round when the live tiles are not a multiple of the grid
+// (192 SwiGLU tiles on 152 SMs: 3 splits make 576 units, 3.8 rounds, against 1.26 rounds of
+// whole tiles that take 2). Split units write fp32 partials to the slab, which holds
+// kMaxGrid x 256 rows of 128 features, so the units of a plan are at most that many blocks of
+// n_max rows; the finishing kernel sums them and runs the epilogue.
 struct SplitPlan {
   int total_rb, live, splits, kps;  // live row blocks, live tiles, splits per tile, K stages per split
   int n_max;                        // rows of the largest row block, rounded up to 32
 };
 
+// Whole warp (every lane must call it).
 __device__ __forceinline__ SplitPlan split_plan(const GemmArgs& a) {
   SplitPlan sp;
   sp.total_rb = 0;
@@ -154,18 +159,30 @@ __device__ __forceinline__ SplitPlan split_plan(const GemmArgs& a) {
   sp.n_max = min(kRowBlock, (rmax + 31) / 32 * 32);
   sp.live = a.n_ftiles * sp.total_rb;
   const int n_k = a.K / kTileK;
-  // up to two work units per CTA when the row blocks are small (the slab then holds at most
-  // 2 grid blocks of 128 rows), otherwise one
-  const int units = sp.n_max <= kRowBlock / 2 ? 2 * a.grid : a.grid;
-  int s = sp.live > 0 ? max(1, min(kMaxSplits, units / sp.live)) : 1;
-  s = min(s, n_k);
-  sp.kps = (n_k + s - 1) / s;
-  sp.splits = (n_k + sp.kps - 1) / sp.kps;  // no empty split
+  uint64_t key = ~0ull;
+  if (sp.live > 0) {
+    const int s = (threadIdx.x & 31) + 1;
+    const int kps = (n_k + s - 1) / s;
+    const int splits = (n_k + kps - 1) / kps;  // no empty split
+    const int units = sp.live * splits;
+    const int cap = kMaxGrid * kRowBlock / sp.n_max;
+    if (splits == 1 || units <= cap) {
+      const int rounds = (units + a.grid - 1) / a.grid;
+      key = (static_cast<uint64_t>(rounds) * static_cast<uint64_t>(kps + 1) << 32) |
+            (static_cast<uint64_t>(splits) << 16) | static_cast<uint64_t>(kps);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, key, off);
+    key = o < key ? o : key;
+  }
+  sp.splits = sp.live > 0 ? static_cast<int>((key >> 16) & 0xFFFFu) : 1;
+  sp.kps = sp.live > 0 ? static_cast<int>(key & 0xFFFFu) : n_k;
   return sp;
 }
 
-// A work unit's block of the slab: n_max rows of 128 fp32 features (the slab holds grid x 256
-// rows, so 2 grid units of at most 128 rows or grid units of 256).
+// A work unit's block of the slab: n_max rows of 128 fp32 features.
 __device__ __forceinline__ float* slab_block(const GemmArgs& a, const SplitPlan& sp, int tile_id, int split) {
   return a.slab + static_cast<int64_t>(tile_id * sp.splits + split) * sp.n_max * kTileM;
 }
@@ -179,13 +196,18 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x,
   const int nvalid = min(32, x.nrows - ch * 32);
   const int64_t rbase = static_cast<int64_t>(x.b) * a.L + x.r0 + ch * 32;
   if constexpr (EPI == kEpiResidual) {
+    // the residual loads of 16 rows are issued before their stores (a store to out0 could
+    // otherwise alias the next load, and the 32 rows would take 32 dependent round trips)
     const int f = x.ft * kTileM + f_in;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      if (c < nvalid) {
-        const int64_t o = (rbase + c) * a.n_out + f;
-        a.out0[o] = to_bf16(v[c] + from_bf16(a.res[o]));
-      }
+    for (int c0 = 0; c0 < 32; c0 += 16) {
+      float rv[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        rv[c] = c0 + c < nvalid ? from_bf16(__ldg(a.res + (rbase + c0 + c) * a.n_out + f)) : 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c0 + c < nvalid) a.out0[(rbase + c0 + c) * a.n_out + f] = to_bf16(v[c0 + c] + rv[c]);
     }
   } else if constexpr (EPI == kEpiSwiglu) {
     bar();  // the exchange buffer is free
@@ -219,13 +241,22 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x,
       bar();
       const int partner = f_in ^ half;  // the rotate-half partner in the same head
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (c < nvalid) {
-          const int pos = min(max(__ldg(a.idx + rbase + c), 0), a.L - 1);  // a bad idx is reported by the norm
-          const float cs = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
-          const float sn = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
-          const float w = sX[c * kXPitch + partner];
-          dst[(rbase + c) * feats + f] = to_bf16(j < half ? v[c] * cs - w * sn : v[c] * cs + w * sn);
+      for (int c0 = 0; c0 < 32; c0 += 16) {
+        // the positions and angles of 16 rows are loaded before their stores
+        float cs[16], sn[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int pos = c0 + c < nvalid ? min(max(__ldg(a.idx + rbase + c0 + c), 0), a.L - 1) : 0;  // a bad idx is reported by the norm
+          cs[c] = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
+          sn[c] = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c0 + c < nvalid) {
+            const float w = sX[(c0 + c) * kXPitch + partner];
+            const float u = v[c0 + c];
+            dst[(rbase + c0 + c) * feats + f] = to_bf16(j < half ? u * cs[c] - w * sn[c] : u * cs[c] + w * sn[c]);
+          }
         }
       }
     }
@@ -414,20 +445,22 @@ __global__ void __launch_bounds__(128) gemm_finish_kernel(GemmArgs a) {
     float v[32];
 #pragma unroll
     for (int c = 0; c < 32; ++c) v[c] = 0.f;
-    float t[kMaxSplits][32];  // every split's values in flight at once before any is added
+    for (int s0 = 0; s0 < sp.splits; s0 += 4) {
+      float t[4][32];  // four splits' values in flight at once before any is added
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      if (s < sp.splits) {
-        const float* blk = slab_block(a, sp, tile_id, s) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
+      for (int s = 0; s < 4; ++s) {
+        if (s0 + s < sp.splits) {
+          const float* blk = slab_block(a, sp, tile_id, s0 + s) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) t[s][c] = blk[c * kTileM];
+          for (int c = 0; c < 32; ++c) t[s][c] = __ldcg(blk + c * kTileM);
+        }
       }
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        if (s0 + s < sp.splits)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] += t[s][c];
     }
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
-      if (s < sp.splits)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] += t[s][c];
     epilogue_chunk<EPI>(a, x, ch, v, sX, f_in, [] { __syncthreads(); });
   }
 }

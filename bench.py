@@ -154,6 +154,17 @@ def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) 
         wt = (torch.randn(w.V, w.d_model, device="cuda", generator=g) / w.d_model ** 0.5).to(torch.bfloat16)
         for _ in range(steps):
             E.lm_head_entropy(hid, wt)
+        del hid, wt
+    if workload == 2:  # and the partial, then the full, forward of one layer of that shape
+        torch.cuda.synchronize()
+        dev = torch.device("cuda", torch.cuda.current_device())
+        lp, lw, x_src, kc, vc, idx_p, R_p, dff, _ = layer_setup(E, dev)
+        lws = E.workspace(E.layer_forward_workspace_size(lp, dff), dev)
+        full_idx = torch.arange(w.L, dtype=torch.int32, device=dev).view(1, w.L)
+        full_R = torch.tensor([w.L], dtype=torch.int32, device=dev)
+        for idx, R in ((idx_p, R_p), (full_idx, full_R)):
+            for _ in range(steps):
+                E.layer_forward(lp, lw, idx, R, x_src, kc, vc, ws=lws)
     torch.cuda.synchronize()
     status, word = E.read_device_error(st.dev_err)
     print(json.dumps({"profile_steps": steps, "R": int(st.R[0]), "flag": int(st.flag[0]), "status": status}))
@@ -620,12 +631,10 @@ def run_trace(E, dev, n_steps) -> dict:
     }
 
 
-def run_layer_forward(E, dev, n_steps) -> dict:
-    """The partial forward of one LLaDA-8B-shaped layer (d 4096, 32 x 128 MHA, d_ff 12288, L 1024)
-    for the headline step's recompute set (R = 95), against the full forward (R = L): the time
-    per layer of the forward each flag selects, and its roofline (weight bytes for the partial
-    forward, tensor-core flops for the full one). Weights drawn on the device at the usual
-    initialisation scale; graph-replayed."""
+def layer_setup(E, dev):
+    """One LLaDA-8B-shaped layer (d 4096, 32 x 128 MHA, d_ff 12288, L 1024; weights drawn on the
+    device at the usual initialisation scale) and the headline step's recompute set, chosen by
+    the library's own select stage: (params, weights, x_src, k, v, idx, R, d_ff, workload)."""
     import torch
 
     w = W.workload(2)
@@ -654,11 +663,23 @@ def run_layer_forward(E, dev, n_steps) -> dict:
            torch.from_numpy(st_h["cand_count"]).to(dev), [], ws=E.workspace(E.step_workspace_size(p), dev))
     torch.cuda.synchronize()
     del base
+    return p, lw, x_src, kc, vc, st.idx, st.R, dff, w
+
+
+def run_layer_forward(E, dev, n_steps) -> dict:
+    """The partial forward of one LLaDA-8B-shaped layer for the headline step's recompute set
+    (R = 95), against the full forward (R = L): the time per layer of the forward each flag
+    selects, and its roofline (weight bytes for the partial forward, tensor-core flops for the
+    full one). Graph-replayed."""
+    import torch
+
+    p, lw, x_src, kc, vc, idx_p, R_p, dff, w = layer_setup(E, dev)
+    d, L, bf = w.Hq * w.D, w.L, torch.bfloat16
     ws = E.workspace(E.layer_forward_workspace_size(p, dff), dev)
     y = torch.empty(1, L, d, dtype=bf, device=dev)
     out = {}
     full_idx = torch.arange(L, dtype=torch.int32, device=dev).view(1, L)
-    for name, idx, R in (("partial", st.idx, st.R), ("full", full_idx, torch.tensor([L], dtype=torch.int32, device=dev))):
+    for name, idx, R in (("partial", idx_p, R_p), ("full", full_idx, torch.tensor([L], dtype=torch.int32, device=dev))):
         n = n_steps if name == "partial" else max(10, n_steps // 8)
         E.layer_forward(p, lw, idx, R, x_src, kc, vc, y=y, ws=ws)
         torch.cuda.synchronize()

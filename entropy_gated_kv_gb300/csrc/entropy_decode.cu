@@ -273,9 +273,23 @@ __device__ __forceinline__ Part reduce_piece(const Piece<DT, LV>& pc) {
   const float M2 = M == -INFINITY ? 0.f : M * kLog2e;
   const uint64_t l2e = f2(kLog2e, kLog2e), nm = f2(-M2, -M2);
   uint64_t sa = 0, sb = 0, ta = 0, tb = 0;  // two accumulator pairs (0 is +0.0f, +0.0f)
+  float q0 = 0.f, q1 = 0.f, r0 = 0.f, r1 = 0.f;  // scalar accumulators (double-width pieces)
 #pragma unroll
   for (int u = 0; u < LV; ++u) {
-    if constexpr (DT == EC_BF16) {
+    if constexpr (DT == EC_BF16 && LV > kLaneVec) {
+      // double-width pieces (the cluster launch) measured faster in scalar fp32 than paired
+      const uint32_t w[4] = {pc.v[u].x, pc.v[u].y, pc.v[u].z, pc.v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t cl = bmax2(w[j], kClampBf16x2);
+        const float dl = fmaf(bf16lo_to_f32(cl), kLog2e, -M2), dh = fmaf(bf16hi_to_f32(cl), kLog2e, -M2);
+        const float pl = ex2_approx(dl), ph = ex2_approx(dh);
+        q0 += pl;
+        q1 += ph;
+        r0 = fmaf(pl, dl, r0);
+        r1 = fmaf(ph, dh, r1);
+      }
+    } else if constexpr (DT == EC_BF16) {
       const uint32_t w[4] = {pc.v[u].x, pc.v[u].y, pc.v[u].z, pc.v[u].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -294,7 +308,7 @@ __device__ __forceinline__ Part reduce_piece(const Piece<DT, LV>& pc) {
   float s0, s1, t0, t1;
   unf2(add2(sa, sb), s0, s1);
   unf2(add2(ta, tb), t0, t1);
-  float S = s0 + s1, T = t0 + t1;
+  float S = s0 + s1 + (q0 + q1), T = t0 + t1 + (r0 + r1);
   if (has_tail) {
     const float d = fmaxf(fmaf(pc.xt, kLog2e, -M2), -127.f);
     const float p = ex2_approx(d);

@@ -38,7 +38,13 @@ namespace {
 
 constexpr int kThreads = 256;  // 8 warps per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kLaneVec = 4;     // 16-byte vectors per lane per piece
+constexpr int kLaneVec = 4;     // 16-byte vectors per lane per piece (the split launch in a step)
+constexpr int kAloneVec = 6;    // the split launch outside a step (many rows: fewer, larger pieces)
+constexpr int kWideVec = 8;     // the cluster launch's double-width pieces
+// Pass 2 in scalar fp32 or on the paired f32x2 instructions, per launch: the form each launch
+// measured faster in (the split launch paired, the cluster launch scalar).
+constexpr bool kSplitScalar = false;
+constexpr bool kWideScalar = true;
 constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
 constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs
 constexpr float kLog2e = 1.4426950408889634f;
@@ -229,7 +235,7 @@ __device__ __forceinline__ float vec_max(const uint4& v) {
 }
 
 // The warp's (max, lowest index, S, T) over one piece; every lane returns it. Whole warp.
-template <int DT, int LV>
+template <int DT, int LV, bool SCALAR>
 __device__ __forceinline__ Part reduce_piece(const Piece<DT, LV>& pc) {
   constexpr int PV = Elem<DT>::kPerVec;
   const int lane = threadIdx.x & 31;
@@ -276,8 +282,7 @@ __device__ __forceinline__ Part reduce_piece(const Piece<DT, LV>& pc) {
   float q0 = 0.f, q1 = 0.f, r0 = 0.f, r1 = 0.f;  // scalar accumulators (double-width pieces)
 #pragma unroll
   for (int u = 0; u < LV; ++u) {
-    if constexpr (DT == EC_BF16 && LV > kLaneVec) {
-      // double-width pieces (the cluster launch) measured faster in scalar fp32 than paired
+    if constexpr (DT == EC_BF16 && SCALAR) {
       const uint32_t w[4] = {pc.v[u].x, pc.v[u].y, pc.v[u].z, pc.v[u].w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -343,8 +348,9 @@ __device__ __forceinline__ void publish_chunk(const EntArgs& a, int row, int chu
   }
 }
 
-// Split path: CTA (row, c) takes chunk c of the row (pieces 8 c .. 8 c + 7, one per warp).
-template <int DT>
+// Split path: CTA (row, c) takes chunk c of the row (pieces 8 c .. 8 c + 7, one per warp, of
+// LV vectors per lane).
+template <int DT, int LV>
 __global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
   __shared__ Part wpart[kWarps];
   pdl_wait();  // logits and row counts may come from the previous kernel in the stream
@@ -352,13 +358,13 @@ __global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
   const int row = static_cast<int>(blockIdx.x) / a.nparts;  // the grid has fewer than 2^31 CTAs
   const int chunk = static_cast<int>(blockIdx.x) - row * a.nparts;
   if (row_skipped(a, row)) return;  // uniform over the CTA
-  const int base = (chunk * kWarps + static_cast<int>(threadIdx.x >> 5)) * piece_elems<DT>();
+  const int base = (chunk * kWarps + static_cast<int>(threadIdx.x >> 5)) * piece_elems<DT, LV>();
   const bool has = base < a.V;  // uniform over the warp
   Part p{};
   if (has) {
-    Piece<DT> pc;
+    Piece<DT, LV> pc;
     load_piece(pc, a.logits + static_cast<int64_t>(row) * a.row_stride_bytes, a.V, base);
-    p = reduce_piece(pc);
+    p = reduce_piece<DT, LV, kSplitScalar>(pc);
   }
   publish_chunk(a, row, chunk, p, has, wpart);
 }
@@ -380,7 +386,7 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
   if (row_skipped(a, row)) return;  // the whole cluster skips the row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const char* rowp = a.logits + static_cast<int64_t>(row) * a.row_stride_bytes;
-  constexpr int LV = 2 * kLaneVec;
+  constexpr int LV = kWideVec;
   constexpr int PE = piece_elems<DT, LV>();
   const int nwide = (a.V + PE - 1) / PE;
   const int per = (nwide + csize - 1) / csize;
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
   for (int piece = p0 + warp; piece < p1; piece += kWarps) {
     Piece<DT, LV> pc;
     load_piece(pc, rowp, a.V, piece * PE);
-    ent_part_merge(acc, reduce_piece(pc));
+    ent_part_merge(acc, reduce_piece<DT, LV, kWideScalar>(pc));
   }
   if (lane == 0) wpart[warp] = acc;
   __syncthreads();
@@ -462,7 +468,7 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   cudaError_t e = current_device_sms(&sms);
   if (e != cudaSuccess) return e;
   // the cluster launch: CTAs of 8 double-width pieces, at most kMaxCluster per row
-  const int64_t wide = kWarps * (f32 ? piece_elems<EC_F32, 2 * kLaneVec>() : piece_elems<EC_BF16, 2 * kLaneVec>());
+  const int64_t wide = kWarps * (f32 ? piece_elems<EC_F32, kWideVec>() : piece_elems<EC_BF16, kWideVec>());
   const int csize = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxCluster, (V + wide - 1) / wide)));
   const int64_t cluster_ctas = static_cast<int64_t>(n_rows) * csize;
   if (!publish_only && (ws == nullptr || (allow_cluster && cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms))) {
@@ -475,10 +481,21 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   const int64_t units = static_cast<int64_t>(n_rows) * np;
   if (units > INT_MAX) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(units));
-  e = f32 ? launch_pdl(entropy_split_kernel<EC_F32>, grid, dim3(kThreads), 0, s, a)
-          : launch_pdl(entropy_split_kernel<EC_BF16>, grid, dim3(kThreads), 0, s, a);
+  // outside a step: chunks of the wider pieces (fewer partials than the workspace holds)
+  const int64_t ce_alone = kWarps * (f32 ? piece_elems<EC_F32, kAloneVec>() : piece_elems<EC_BF16, kAloneVec>());
+  EntArgs a_alone = a;
+  a_alone.nparts = static_cast<int32_t>((static_cast<int64_t>(V) + ce_alone - 1) / ce_alone);
+  const dim3 grid_alone(static_cast<unsigned>(static_cast<int64_t>(n_rows) * a_alone.nparts));
+  // inside a step (publish only) the pieces have the width the select kernel's merge expects;
+  // outside, many rows take the wider pieces (measured faster at 78 MB, slower in the step)
+  if (publish_only)
+    e = f32 ? launch_pdl(entropy_split_kernel<EC_F32, kLaneVec>, grid, dim3(kThreads), 0, s, a)
+            : launch_pdl(entropy_split_kernel<EC_BF16, kLaneVec>, grid, dim3(kThreads), 0, s, a);
+  else
+    e = f32 ? launch_pdl(entropy_split_kernel<EC_F32, kAloneVec>, grid_alone, dim3(kThreads), 0, s, a_alone)
+            : launch_pdl(entropy_split_kernel<EC_BF16, kAloneVec>, grid_alone, dim3(kThreads), 0, s, a_alone);
   if (e != cudaSuccess || publish_only) return e;
-  return launch_pdl(entropy_merge_kernel, dim3((n_rows + 7) / 8), dim3(256), 0, s, a);
+  return launch_pdl(entropy_merge_kernel, dim3((n_rows + 7) / 8), dim3(256), 0, s, a_alone);
 }
 
 }  // namespace ec

@@ -515,6 +515,12 @@ def summarise_config(w, steps_per_s, flag, R, kern, per_copy_bytes, inputs) -> d
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     intensity = alg["partial_attention_flops"] / alg["partial_attention_bytes"]
     att_bound = "tensor" if intensity > ridge else "hbm"
+    extra = {}
+    if "dense_attention_us" in kern:  # the SM-pair kernel on the same full step
+        d_tfs = alg["partial_attention_flops"] / (kern["dense_attention_us"] * 1e6)
+        extra["dense_attention"] = {"us": kern["dense_attention_us"], "TFLOP/s": d_tfs,
+                                    "frac_bf16": d_tfs / pk["bf16_tflops"],
+                                    "kernel": "ec_dense_attention (2-CTA products on SM pairs)"}
     return {
         "workload": workload_desc(w),
         "step": f"{'full' if flag else 'partial'} (R={R} over the batch)",
@@ -534,6 +540,7 @@ def summarise_config(w, steps_per_s, flag, R, kern, per_copy_bytes, inputs) -> d
                               else att_gbs / pk["hbm_gbs"]},
         "kv_scatter": {"us": kern["kv_scatter_us"]},
         "decision_us": kern["entropy_decode_us"],
+        **extra,
     }
 
 
@@ -814,6 +821,12 @@ def time_kernels(E, p, w, copies, st0, dev, n, lm_head=True) -> dict:
     out["entropy_decode_us"] = timed(stage_entropy, n)
     out["read_floor_us"] = timed(stage_floor, n)
     out["partial_attention_us"] = timed(stage_attention, n)
+    if int(R.sum().item()) == w.B * w.L and w.D == 128:  # a full step: the SM-pair dense kernel too
+        def stage_dense(i):
+            kc, vc = kv_rot[i % n_kv]
+            E.dense_attention(p, qfull, kc, vc, att_out)
+
+        out["dense_attention_us"] = timed(stage_dense, n)
     out["kv_scatter_us"] = timed(stage_scatter, n)
     out["R"] = int(R.sum().item())  # recompute rows over the batch
     out["rotations"] = {"steps": nc, "logits": n_lg, "kv_cache": n_kv}

@@ -262,6 +262,17 @@ def partial_attention(p: Params, q, k_cache, v_cache, R, out, scale: float | Non
     return out
 
 
+def dense_attention(p: Params, q, k_cache, v_cache, out, scale: float | None = None, dev_err=None, stream=None):
+    """(d) for a step known to be full: out[b, r, h] = softmax(scale q k^T) v over all L keys for
+    every position r (q in position order), on SM pairs with 2-CTA products; D = 128."""
+    pc = p.c()
+    sc = (1.0 / math.sqrt(p.D)) if scale is None else float(scale)
+    st = lib().ec_dense_attention(ctypes.byref(pc), _vp(q), _vp(k_cache), _vp(v_cache), sc, _vp(out), _vp(dev_err),
+                                  _stream(stream))
+    C.check(st, "ec_dense_attention")
+    return out
+
+
 @dataclass
 class LayerWeights:
     """Weights of one LLaMA-style layer for layer_forward (ec_layer): CUDA bf16 tensors wq

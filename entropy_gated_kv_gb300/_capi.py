@@ -78,6 +78,7 @@ SIGNATURES: dict[str, tuple] = {
     "ec_kv_scatter": (_i32, [ctypes.POINTER(EcParams), _p, _p, _p, _p, _i32, _p, _p, _p, _p]),
     "ec_partial_attention_workspace_size": (_sz, [ctypes.POINTER(EcParams)]),
     "ec_partial_attention": (_i32, [ctypes.POINTER(EcParams), _p, _p, _p, _p, _f32, _p, _p, _sz, _p, _p]),
+    "ec_dense_attention": (_i32, [ctypes.POINTER(EcParams), _p, _p, _p, _f32, _p, _p, _p]),
     "ec_step_workspace_size": (_sz, [ctypes.POINTER(EcParams)]),
     "ec_step": (_i32, [ctypes.POINTER(EcParams), ctypes.POINTER(EcState), _p, _p, _p, _i32,
                        ctypes.POINTER(_p), ctypes.POINTER(_p), ctypes.POINTER(_p), ctypes.POINTER(_p),

@@ -274,6 +274,19 @@ size_t ec_partial_attention_workspace_size(const ec_params* p) {
   return attention_workspace_bytes(*p);
 }
 
+ec_status ec_dense_attention(const ec_params* p, const void* q, const void* k_cache, const void* v_cache,
+                             float scale, void* out, int32_t* dev_err, ec_stream_t stream) {
+  ec_status r = check_params(p, kCheckAttn);
+  if (r != EC_OK) return r;
+  if (!q || !k_cache || !v_cache || !out) return EC_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return EC_ERR_INVALID_ARG;
+  if (!(scale == scale)) return EC_ERR_INVALID_ARG;
+  if (p->D != 128) return EC_ERR_UNSUPPORTED;
+  ec_status st = EC_OK;
+  launch_dense_attention(*p, q, k_cache, v_cache, scale, out, dev_err, static_cast<cudaStream_t>(stream), &st);
+  return st;
+}
+
 ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* R, float scale, void* out, void* ws, size_t ws_bytes,
                                int32_t* dev_err, ec_stream_t stream) {

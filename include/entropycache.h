@@ -16,6 +16,7 @@
  *                                                  -> ec_kv_scatter
  *   (d) bidirectional attention of the recompute rows against all L cached rows
  *                                                  -> ec_partial_attention
+ *       (or, for a step known to be full, of every row: ec_dense_attention)
  *   ec_step runs (a)(b)(c) once and then (c-scatter)(d) for every layer.
  *
  * Beyond the step: ec_layer_forward runs the partial (or full) forward of one transformer layer
@@ -323,6 +324,20 @@ size_t ec_partial_attention_workspace_size(const ec_params* p);
 ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* R, float scale, void* out,
                                void* ws, size_t ws_bytes, int32_t* dev_err, ec_stream_t stream);
+
+/* ---- (d) dense attention for a step known to be full --------------------------------------
+ * Every position attends to every cached key (the full recompute of the pt summary §2
+ * "Decisão de Pulo"; no mask, zh summary §1). The same result as ec_partial_attention with
+ * R[b] = L and q in position order, for the steps a caller knows are full before they run
+ * (the first forward of each generation block is full by definition), on pairs of SMs
+ * with 2-CTA tensor-core products (each product covers two 128-row tiles, each SM loads half
+ * of every K/V block). For b < B, position r < L, query head h (kv head h / (Hq / Hkv)):
+ *   out[b, r, h, :] = sum_j softmax_j(scale * <q[b, r, h, :], k_cache[b, j, h/g, :]>) v_cache[b, j, h/g, :]
+ * q, out bf16 [B, L, Hq, D]; k_cache, v_cache bf16 [B, L, Hkv, D]; D = 128 (other head
+ * sizes return EC_ERR_UNSUPPORTED). No workspace. Rounding as ec_partial_attention. A
+ * pipeline wait that exceeds its limit sets EC_DEVERR_TIMEOUT in dev_err (if given). */
+ec_status ec_dense_attention(const ec_params* p, const void* q, const void* k_cache, const void* v_cache,
+                             float scale, void* out, int32_t* dev_err, ec_stream_t stream);
 
 /* ---- the partial forward of one transformer layer ------------------------------------------
  * The forward pass the step's flag selects (EntropyCache, gist.science zh summary §2.2,

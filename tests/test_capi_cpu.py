@@ -111,6 +111,26 @@ def test_partial_attention_rejects_bad_args(capi):
     assert f(ctypes.byref(good), p, p, p, p, float("nan"), p, p, big, None, None) == capi.EC_ERR_INVALID_ARG
 
 
+def test_dense_attention_rejects_bad_args(capi):
+    lib = capi.load()
+    f = lib.ec_dense_attention
+    p = ctypes.c_void_p(FAKE)
+    good = _params(capi, D=128)
+    for bad, want in [
+        (_params(capi, D=128, Hkv=5), capi.EC_ERR_INVALID_ARG),  # Hq % Hkv
+        (_params(capi, D=64), capi.EC_ERR_UNSUPPORTED),  # the pair kernel splits V's 128 dims
+        (_params(capi, D=96), capi.EC_ERR_UNSUPPORTED),
+        (_params(capi, D=128, B=0), capi.EC_ERR_INVALID_ARG),
+        (_params(capi, D=128, L=0), capi.EC_ERR_INVALID_ARG),
+    ]:
+        assert f(ctypes.byref(bad), p, p, p, 0.1, p, None, None) == want
+    assert f(None, p, p, p, 0.1, p, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), None, p, p, 0.1, p, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), p, p, p, 0.1, None, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), p, ctypes.c_void_p(FAKE + 8), p, 0.1, p, None, None) == capi.EC_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), p, p, p, float("nan"), p, None, None) == capi.EC_ERR_INVALID_ARG
+
+
 def test_select_and_scatter_reject_bad_args(capi):
     lib = capi.load()
     p = ctypes.c_void_p(FAKE)

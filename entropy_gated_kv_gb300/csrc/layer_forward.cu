@@ -187,38 +187,40 @@ __device__ __forceinline__ float* slab_block(const GemmArgs& a, const SplitPlan&
   return a.slab + static_cast<int64_t>(tile_id * sp.splits + split) * sp.n_max * kTileM;
 }
 
-// The fused epilogue of 32 rows (chunk ch of tile x) of one output feature per thread: v[c] is
-// the accumulator of row 32 ch + c. All 128 threads of the epilogue call it; bar() synchronises
+// The fused epilogue of ROWS rows (rows row0 .. row0 + ROWS - 1 of tile x) of one output
+// feature per thread: v[c] is the accumulator of row row0 + c. All 128 threads of the epilogue call it; bar() synchronises
 // them (the exchange buffer sX carries the RoPE partner or the SwiGLU up value).
-template <int EPI, typename Bar>
-__device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x, int ch, const float (&v)[32],
-                                               float* sX, int f_in, Bar bar) {
-  const int nvalid = min(32, x.nrows - ch * 32);
-  const int64_t rbase = static_cast<int64_t>(x.b) * a.L + x.r0 + ch * 32;
+template <int EPI, int ROWS, typename Bar>
+__device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const Tile& x, int row0, const float (&v)[ROWS],
+                                              float* sX, int f_in, Bar bar) {
+  static_assert(ROWS <= 32 && ROWS % 8 == 0, "the exchange buffer holds 32 rows");
+  constexpr int G = ROWS < 16 ? ROWS : 16;  // rows whose loads are issued before their stores
+  const int nvalid = min(ROWS, x.nrows - row0);
+  const int64_t rbase = static_cast<int64_t>(x.b) * a.L + x.r0 + row0;
   if constexpr (EPI == kEpiResidual) {
-    // the residual loads of 16 rows are issued before their stores (a store to out0 could
-    // otherwise alias the next load, and the 32 rows would take 32 dependent round trips)
+    // the residual loads of G rows are issued before their stores (a store to out0 could
+    // otherwise alias the next load, and the rows would take one dependent round trip each)
     const int f = x.ft * kTileM + f_in;
 #pragma unroll
-    for (int c0 = 0; c0 < 32; c0 += 16) {
-      float rv[16];
+    for (int c0 = 0; c0 < ROWS; c0 += G) {
+      float rv[G];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < G; ++c)
         rv[c] = c0 + c < nvalid ? from_bf16(__ldg(a.res + (rbase + c0 + c) * a.n_out + f)) : 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < G; ++c)
         if (c0 + c < nvalid) a.out0[(rbase + c0 + c) * a.n_out + f] = to_bf16(v[c0 + c] + rv[c]);
     }
   } else if constexpr (EPI == kEpiSwiglu) {
     bar();  // the exchange buffer is free
     if (f_in >= 64)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = v[c];
+      for (int c = 0; c < ROWS; ++c) sX[c * kXPitch + f_in] = v[c];
     bar();
     if (f_in < 64) {
       const int f = x.ft * 64 + f_in;
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
+      for (int c = 0; c < ROWS; ++c)
         if (c < nvalid) a.out0[(rbase + c) * a.n_out + f] = to_bf16(silu(v[c]) * sX[c * kXPitch + f_in + 64]);
     }
   } else {  // q / k with RoPE, v as is
@@ -229,7 +231,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x,
     const int f = f0 - (part == 0 ? 0 : (part == 1 ? a.q_feats : a.q_feats + a.kv_feats)) + f_in;
     if (part == 2) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
+      for (int c = 0; c < ROWS; ++c)
         if (c < nvalid) dst[(rbase + c) * feats + f] = to_bf16(v[c]);
     } else {
       const int half = a.D / 2;
@@ -237,21 +239,21 @@ __device__ __forceinline__ void epilogue_chunk(const GemmArgs& a, const Tile& x,
       const int i = j % half;
       bar();  // the exchange buffer is free
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sX[c * kXPitch + f_in] = v[c];
+      for (int c = 0; c < ROWS; ++c) sX[c * kXPitch + f_in] = v[c];
       bar();
       const int partner = f_in ^ half;  // the rotate-half partner in the same head
 #pragma unroll
-      for (int c0 = 0; c0 < 32; c0 += 16) {
-        // the positions and angles of 16 rows are loaded before their stores
-        float cs[16], sn[16];
+      for (int c0 = 0; c0 < ROWS; c0 += G) {
+        // the positions and angles of G rows are loaded before their stores
+        float cs[G], sn[G];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < G; ++c) {
           const int pos = c0 + c < nvalid ? min(max(__ldg(a.idx + rbase + c0 + c), 0), a.L - 1) : 0;  // a bad idx is reported by the norm
           cs[c] = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
           sn[c] = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
         }
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < G; ++c) {
           if (c0 + c < nvalid) {
             const float w = sX[(c0 + c) * kXPitch + partner];
             const float u = v[c0 + c];
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
         if (sp.splits == 1) {
-          epilogue_chunk<EPI>(a, x, ch, v, sX, f_in, [] { named_bar_sync(1, 128); });
+          epilogue_rows<EPI, 32>(a, x, ch * 32, v, sX, f_in, [] { named_bar_sync(1, 128); });
         } else {  // a split's partial: rows of 128 fp32 features, coalesced
           float* blk = slab_block(a, sp, tile_id, split) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
 #pragma unroll
@@ -427,41 +429,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   }
 }
 
-// Sums the split-K partials of each (tile, 32-row chunk) and runs the fused epilogue; nothing
-// when the GEMM ran unsplit. 128 threads, one output feature each.
+// Sums the split-K partials of each (tile, 8-row group) and runs the fused epilogue; nothing
+// when the GEMM ran unsplit. 128 threads, one output feature each. The items are small (8 rows,
+// the partials of up to 8 splits in flight at once), so many CTAs share an SM and an item takes
+// one round trip per 8 splits.
+constexpr int kFinRows = 8;
+constexpr int kFinSplits = 8;
+
 template <int EPI>
 __global__ void __launch_bounds__(128) gemm_finish_kernel(GemmArgs a) {
-  __shared__ float sX[32 * kXPitch];
+  __shared__ float sX[kFinRows * kXPitch];
   pdl_wait();  // the partials come from the GEMM
   pdl_launch_dependents();
   const SplitPlan sp = split_plan(a);
   if (sp.splits == 1) return;
   const int f_in = threadIdx.x;
-  const int items = sp.live * (kRowBlock / 32);
+  const int groups = sp.n_max / kFinRows;  // groups of the largest row block
+  const int items = sp.live * groups;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {  // uniform over the CTA
-    const int tile_id = it / (kRowBlock / 32), ch = it - tile_id * (kRowBlock / 32);
+    const int tile_id = it / groups, grp = it - tile_id * groups;
     const Tile x = decode_tile(tile_id, sp.total_rb, a);
-    if (ch * 32 >= x.nrows) continue;
-    float v[32];
+    if (grp * kFinRows >= x.nrows) continue;
+    float v[kFinRows];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) v[c] = 0.f;
-    for (int s0 = 0; s0 < sp.splits; s0 += 4) {
-      float t[4][32];  // four splits' values in flight at once before any is added
+    for (int c = 0; c < kFinRows; ++c) v[c] = 0.f;
+    for (int s0 = 0; s0 < sp.splits; s0 += kFinSplits) {
+      float t[kFinSplits][kFinRows];  // the splits' values in flight at once before any is added
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
+      for (int s = 0; s < kFinSplits; ++s) {
         if (s0 + s < sp.splits) {
-          const float* blk = slab_block(a, sp, tile_id, s0 + s) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
+          const float* blk = slab_block(a, sp, tile_id, s0 + s) + static_cast<int64_t>(grp * kFinRows) * kTileM + f_in;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) t[s][c] = __ldcg(blk + c * kTileM);
+          for (int c = 0; c < kFinRows; ++c) t[s][c] = __ldcg(blk + c * kTileM);
         }
       }
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
+      for (int s = 0; s < kFinSplits; ++s)
         if (s0 + s < sp.splits)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] += t[s][c];
+          for (int c = 0; c < kFinRows; ++c) v[c] += t[s][c];
     }
-    epilogue_chunk<EPI>(a, x, ch, v, sX, f_in, [] { __syncthreads(); });
+    epilogue_rows<EPI, kFinRows>(a, x, grp * kFinRows, v, sX, f_in, [] { __syncthreads(); });
   }
 }
 
@@ -587,7 +595,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   g.grid = std::max(1, std::min(sms, kMaxGrid));
   e = launch_pdl(gemm_kernel<EPI>, dim3(g.grid), dim3(kThreads), kSmemBytes, s, a0, a1, a2, x, g);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_finish_kernel<EPI>, dim3(4 * g.grid), dim3(128), 0, s, g);
+  return launch_pdl(gemm_finish_kernel<EPI>, dim3(8 * g.grid), dim3(128), 0, s, g);
 }
 
 }  // namespace

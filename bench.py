@@ -117,7 +117,7 @@ def profiled_traffic(kernel: str, source: str) -> float | None:
 def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) -> None:
     """A few eager steps of the workload (no graphs, no timing), then as many calls of the
     standalone decode entry on the step's logits and of the output projection fused with the
-    decode: a short program for ncu."""
+    decode (on a full step, of the SM-pair dense attention first): a short program for ncu."""
     import torch
 
     import entropy_gated_kv_gb300 as E
@@ -144,6 +144,9 @@ def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) 
         st = E.DecodeState.from_arrays(p, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
                                        ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
         E.step(p, st, logits, cp, cc, [layer], ws=ws)
+    if int(st.flag.max().item()) and w.D == 128:  # a full step: also the SM-pair dense attention
+        for _ in range(steps):
+            E.dense_attention(p, layer["q_src"], layer["k_cache"], layer["v_cache"], layer["out"])
     rows = logits.view(-1, w.V)
     ews = E.workspace(E.entropy_decode_workspace_size(rows.shape[0], w.V, rows.dtype))
     for _ in range(steps):

@@ -69,7 +69,8 @@ struct GemmBars {
 };
 
 constexpr uint32_t kXOff = kRingBytes;
-constexpr uint32_t kBarOff = kXOff + 32 * kXPitch * 4;
+constexpr uint32_t kPosOff = kXOff + 32 * kXPitch * 4;  // the tile's row positions (qkv epilogue)
+constexpr uint32_t kBarOff = kPosOff + kRowBlock * 4;
 constexpr uint32_t kSmemBytes = kBarOff + sizeof(GemmBars) + 1024;  // + slack for 1024-byte alignment
 
 struct GemmArgs {
@@ -190,9 +191,11 @@ __device__ __forceinline__ float* slab_block(const GemmArgs& a, const SplitPlan&
 // The fused epilogue of ROWS rows (rows row0 .. row0 + ROWS - 1 of tile x) of one output
 // feature per thread: v[c] is the accumulator of row row0 + c. All 128 threads of the epilogue call it; bar() synchronises
 // them (the exchange buffer sX carries the RoPE partner or the SwiGLU up value).
+// spos (may be null): the positions of these rows, already in shared memory (the qkv epilogue
+// reads them instead of idx).
 template <int EPI, int ROWS, typename Bar>
 __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const Tile& x, int row0, const float (&v)[ROWS],
-                                              float* sX, int f_in, Bar bar) {
+                                              float* sX, int f_in, Bar bar, const int* spos = nullptr) {
   static_assert(ROWS <= 32 && ROWS % 8 == 0, "the exchange buffer holds 32 rows");
   constexpr int G = ROWS < 16 ? ROWS : 16;  // rows whose loads are issued before their stores
   const int nvalid = min(ROWS, x.nrows - row0);
@@ -248,7 +251,9 @@ __device__ __forceinline__ void epilogue_rows(const GemmArgs& a, const Tile& x, 
         float cs[G], sn[G];
 #pragma unroll
         for (int c = 0; c < G; ++c) {
-          const int pos = c0 + c < nvalid ? min(max(__ldg(a.idx + rbase + c0 + c), 0), a.L - 1) : 0;  // a bad idx is reported by the norm
+          const int pos = c0 + c >= nvalid ? 0
+                          : spos != nullptr ? spos[c0 + c]
+                                            : min(max(__ldg(a.idx + rbase + c0 + c), 0), a.L - 1);  // a bad idx is reported by the norm
           cs[c] = __ldg(a.rope_cos + static_cast<int64_t>(pos) * half + i);
           sn[c] = __ldg(a.rope_sin + static_cast<int64_t>(pos) * half + i);
         }
@@ -274,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   GemmBars* bars = reinterpret_cast<GemmBars*>(smem + kBarOff);
   float* sX = reinterpret_cast<float*>(smem + kXOff);
+  int* sPos = reinterpret_cast<int*>(smem + kPosOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_k = a.K / kTileK;
   (void)n_k;
@@ -395,6 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // be left at a named barrier that the others have abandoned
       named_bar_sync(1, 128);
       if (et == 0) bars->epi_ok = mbar_wait_bounded(&bars->acc_full[buf], use & 1u, abort_flag, a.dev_err, kWaitLimitNs) ? 1 : 0;
+      if constexpr (EPI == kEpiQkv) {  // the tile's positions for RoPE, once (the previous tile's reads are done)
+        if (sp.splits == 1)
+          for (int r = et; r < x.nrows; r += 128)
+            sPos[r] = min(max(__ldg(a.idx + static_cast<int64_t>(x.b) * a.L + x.r0 + r), 0), a.L - 1);
+      }
       named_bar_sync(1, 128);
       if (!bars->epi_ok) break;
       tc_fence_after();
@@ -410,7 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
         for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r[c]);
         if (sp.splits == 1) {
-          epilogue_rows<EPI, 32>(a, x, ch * 32, v, sX, f_in, [] { named_bar_sync(1, 128); });
+          epilogue_rows<EPI, 32>(a, x, ch * 32, v, sX, f_in, [] { named_bar_sync(1, 128); },
+                                 EPI == kEpiQkv ? sPos + ch * 32 : nullptr);
         } else {  // a split's partial: rows of 128 fp32 features, coalesced
           float* blk = slab_block(a, sp, tile_id, split) + static_cast<int64_t>(ch * 32) * kTileM + f_in;
 #pragma unroll

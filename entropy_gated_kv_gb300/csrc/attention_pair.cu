@@ -23,7 +23,9 @@
 //               TMEM, and commits to barriers in both CTAs at once (multicast).
 //   warps 2..5  softmax and epilogue for this CTA's 128 rows, as in the partial-attention kernel
 //               (one TMEM lane per row, lazy rescale, P written over the S buffer); each warp tells
-//               the leader when its P rows (and, per item, its O rows) are done.
+//               the leader when its P rows (and, per item, its O rows) are done: in the leader
+//               directly, in the peer through a local barrier whose completion the peer's warp 1
+//               forwards with one remote arrival (cheaper than four warps arriving remotely).
 // GQA packs the g query heads of a KV head into the 128 rows (floor(128 / g) positions per tile).
 // Every wait is bounded and reports EC_DEVERR_TIMEOUT.
 #include <cuda.h>
@@ -41,7 +43,7 @@ constexpr int D = 128;           // head size (V is split by dims over the pair:
 constexpr int kBlockM = 128;     // packed query rows per CTA tile (TMEM lanes)
 constexpr int kBlockN = 128;     // keys per block
 constexpr int kHalfN = 64;       // keys of K (and dims of V) each CTA loads per block
-constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 softmax + epilogue
+constexpr int kThreads = 192;    // warp 0 TMA, warp 1 MMA (the peer's: P relay), warps 2-5 softmax + epilogue
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBuf = 3;         // S/P buffers in TMEM
 constexpr int kKvStages = 5;     // K/V stages in shared memory
@@ -65,8 +67,9 @@ struct Bars {
   uint64_t q_full, q_empty;                      // q_full: leader only (both tiles' bytes)
   uint64_t kv_full[kKvStages], kv_empty[kKvStages];  // kv_full: leader only (both halves' bytes)
   uint64_t s_full[kSBuf], s_free[kSBuf];
-  uint64_t p_full[kSBuf];                        // leader only: 8 warps of the pair
-  uint64_t o_full, o_free;                       // o_free: leader only: 8 warps of the pair
+  uint64_t p_full[kSBuf];                        // leader only: its 4 softmax warps + the peer's relay
+  uint64_t o_full, o_free;                       // o_free: leader only: its 4 softmax warps + the peer's relay
+  uint64_t p_local[kSBuf], o_local;              // peer only: its 4 softmax warps, relayed to the leader
   uint32_t tmem_base;
   int abort;
 };
@@ -156,15 +159,16 @@ EC_DEV bool wait_cluster_bounded(uint64_t* bar, uint32_t parity, volatile int* a
   }
 }
 
-// One arrival of this warp on a barrier in the leader's shared memory (lane 0, after the warp's
-// preceding tensor-memory stores were fenced).
-EC_DEV void arrive_leader(uint64_t* bar, uint32_t rank) {
-  if (rank == 0) {
-    mbar_arrive(bar);
-  } else {
-    const uint32_t remote = dsmem_map(smem_u32(bar), 0);
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
-  }
+// One arrival of a warp that has finished its rows (lane 0, after the warp's preceding
+// tensor-memory stores were fenced): in the leader on the leader's barrier; in the peer on the
+// peer's local barrier, which the peer's relay thread forwards to the leader with one remote
+// arrival (the warps' own arrivals stay local and cheap; release/acquire order is transitive).
+EC_DEV void arrive_done(uint64_t* leader_bar, uint64_t* local_bar, uint32_t rank) {
+  mbar_arrive(rank == 0 ? leader_bar : local_bar);
+}
+EC_DEV void arrive_remote_leader(uint64_t* bar) {
+  const uint32_t remote = dsmem_map(smem_u32(bar), 0);
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 struct PairItem {
@@ -214,10 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) pair_attention_kernel(
     for (int i = 0; i < kSBuf; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 1);
-      mbar_init(&bars->p_full[i], 8);
+      mbar_init(&bars->p_full[i], 5);
+      mbar_init(&bars->p_local[i], 4);
     }
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_free, 8);
+    mbar_init(&bars->o_free, 5);
+    mbar_init(&bars->o_local, 4);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -329,6 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1) pair_attention_kernel(
         const uint32_t peer_abort = dsmem_map(smem_u32(&bars->abort), 1);
         asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1) : "memory");
       }
+    } else if (rank == 1 && lane == 0) {
+      // relay: the peer's softmax warps finished a block's P (or an item's O): one remote arrival
+      bool ok = true;
+      uint32_t it = 0;
+      for (int n = 0; ok; ++n) {
+        const int item = cluster + n * nclusters;
+        if (item >= n_items) break;
+        for (int j = 0; ok && j < nblk; ++j) {
+          const uint32_t cur = it + j, sb = cur % kSBuf, su = cur / kSBuf;
+          ok = mbar_wait_bounded(&bars->p_local[sb], su & 1u, abort_flag, dev_err, kWaitLimitNs);
+          if (ok) arrive_remote_leader(&bars->p_full[sb]);
+        }
+        it += nblk;
+        ok = ok && mbar_wait_bounded(&bars->o_local, n & 1, abort_flag, dev_err, kWaitLimitNs);
+        if (ok) arrive_remote_leader(&bars->o_free);
+      }
     }
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
@@ -411,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_attention_kernel(
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_leader(&bars->p_full[sb], rank);
+        if (lane == 0) arrive_done(&bars->p_full[sb], &bars->p_local[sb], rank);
       }
       it += nblk;
       if (ok) ok = mbar_wait_bounded(&bars->o_full, n & 1, abort_flag, dev_err, kWaitLimitNs);
@@ -442,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_attention_kernel(
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_leader(&bars->o_free, rank);
+      if (lane == 0) arrive_done(&bars->o_free, &bars->o_local, rank);
     }
   }
 

@@ -117,7 +117,7 @@ def profiled_traffic(kernel: str, source: str) -> float | None:
 def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) -> None:
     """A few eager steps of the workload (no graphs, no timing), then as many calls of the
     standalone decode entry on the step's logits and of the output projection fused with the
-    decode (on a full step, of the SM-pair dense attention first): a short program for ncu."""
+    decode (on a full step, of the dense attention first): a short program for ncu."""
     import torch
 
     import entropy_gated_kv_gb300 as E
@@ -144,7 +144,7 @@ def run_profile(steps: int, workload: int = WORKLOAD, tau: float | None = None) 
         st = E.DecodeState.from_arrays(p, tokens=st_h["tokens"], mask=st_h["mask"], ring=st_h["ring"],
                                        ring_head=st_h["ring_head"], ring_count=st_h["ring_count"])
         E.step(p, st, logits, cp, cc, [layer], ws=ws)
-    if int(st.flag.max().item()) and w.D == 128:  # a full step: also the SM-pair dense attention
+    if int(st.flag.max().item()) and w.D == 128:  # a full step: also the dense attention
         for _ in range(steps):
             E.dense_attention(p, layer["q_src"], layer["k_cache"], layer["v_cache"], layer["out"])
     rows = logits.view(-1, w.V)
@@ -519,11 +519,11 @@ def summarise_config(w, steps_per_s, flag, R, kern, per_copy_bytes, inputs) -> d
     intensity = alg["partial_attention_flops"] / alg["partial_attention_bytes"]
     att_bound = "tensor" if intensity > ridge else "hbm"
     extra = {}
-    if "dense_attention_us" in kern:  # the SM-pair kernel on the same full step
+    if "dense_attention_us" in kern:  # the two-tile dense kernel on the same full step
         d_tfs = alg["partial_attention_flops"] / (kern["dense_attention_us"] * 1e6)
         extra["dense_attention"] = {"us": kern["dense_attention_us"], "TFLOP/s": d_tfs,
                                     "frac_bf16": d_tfs / pk["bf16_tflops"],
-                                    "kernel": "ec_dense_attention (2-CTA products on SM pairs)"}
+                                    "kernel": "ec_dense_attention (two query tiles per CTA, a softmax warpgroup each)"}
     return {
         "workload": workload_desc(w),
         "step": f"{'full' if flag else 'partial'} (R={R} over the batch)",
@@ -824,7 +824,7 @@ def time_kernels(E, p, w, copies, st0, dev, n, lm_head=True) -> dict:
     out["entropy_decode_us"] = timed(stage_entropy, n)
     out["read_floor_us"] = timed(stage_floor, n)
     out["partial_attention_us"] = timed(stage_attention, n)
-    if int(R.sum().item()) == w.B * w.L and w.D == 128:  # a full step: the SM-pair dense kernel too
+    if int(R.sum().item()) == w.B * w.L and w.D == 128:  # a full step: the dense kernel too
         def stage_dense(i):
             kc, vc = kv_rot[i % n_kv]
             E.dense_attention(p, qfull, kc, vc, att_out)

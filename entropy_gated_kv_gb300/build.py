@@ -21,7 +21,7 @@ BUILD = PKG / "_build"
 LIB_NAME = "libentropycache.so"
 LIB_PATH = PKG / LIB_NAME
 
-SOURCES = ["entropy_decode.cu", "select_recompute.cu", "kv_scatter.cu", "attention.cu", "attention_pair.cu", "ec_api.cu",
+SOURCES = ["entropy_decode.cu", "select_recompute.cu", "kv_scatter.cu", "attention.cu", "attention_dense.cu", "ec_api.cu",
            "entropy_decode_noalloc.cu", "lm_head_entropy.cu", "layer_forward.cu",
            "read_floor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

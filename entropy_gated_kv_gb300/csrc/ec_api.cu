@@ -283,7 +283,7 @@ ec_status ec_dense_attention(const ec_params* p, const void* q, const void* k_ca
   if (!(scale == scale)) return EC_ERR_INVALID_ARG;
   if (p->D != 128) return EC_ERR_UNSUPPORTED;
   ec_status st = EC_OK;
-  launch_dense_attention(*p, q, k_cache, v_cache, scale, out, dev_err, static_cast<cudaStream_t>(stream), &st);
+  launch_dense_attention_tiles(*p, q, k_cache, v_cache, scale, out, dev_err, static_cast<cudaStream_t>(stream), &st);
   return st;
 }
 

@@ -75,9 +75,11 @@ cudaError_t launch_partial_attention(const ec_params& p, const void* q, const vo
                                      const void* v_cache, const int32_t* R, float scale, void* out, void* ws,
                                      int32_t* dev_err, bool plan_early, cudaStream_t s, ec_status* status);
 
-// ---- dense attention on SM pairs (attention_pair.cu): every position against every key ---
-cudaError_t launch_dense_attention(const ec_params& p, const void* q, const void* k_cache, const void* v_cache,
-                                   float scale, void* out, int32_t* dev_err, cudaStream_t s, ec_status* status);
+// ---- dense attention, two query tiles per CTA (attention_dense.cu): every position against
+// every key ---------------------------------------------------------------------------------
+cudaError_t launch_dense_attention_tiles(const ec_params& p, const void* q, const void* k_cache, const void* v_cache,
+                                         float scale, void* out, int32_t* dev_err, cudaStream_t s,
+                                         ec_status* status);
 
 // ---- the partial forward of one layer (layer_forward.cu) ----------------------------------
 size_t layer_forward_workspace_bytes(const ec_params& p, int32_t d_ff);

@@ -329,9 +329,10 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
  * Every position attends to every cached key (the full recompute of the pt summary §2
  * "Decisão de Pulo"; no mask, zh summary §1). The same result as ec_partial_attention with
  * R[b] = L and q in position order, for the steps a caller knows are full before they run
- * (the first forward of each generation block is full by definition), on pairs of SMs
- * with 2-CTA tensor-core products (each product covers two 128-row tiles, each SM loads half
- * of every K/V block). For b < B, position r < L, query head h (kv head h / (Hq / Hkv)):
+ * (the first forward of each generation block is full by definition): each CTA takes two
+ * 128-row query tiles that share every K/V block, with a softmax warpgroup per tile, so one
+ * tile's softmax overlaps the other's tensor-core products. For b < B, position r < L, query
+ * head h (kv head h / (Hq / Hkv)):
  *   out[b, r, h, :] = sum_j softmax_j(scale * <q[b, r, h, :], k_cache[b, j, h/g, :]>) v_cache[b, j, h/g, :]
  * q, out bf16 [B, L, Hq, D]; k_cache, v_cache bf16 [B, L, Hkv, D]; D = 128 (other head
  * sizes return EC_ERR_UNSUPPORTED). No workspace. Rounding as ec_partial_attention. A

@@ -1,11 +1,11 @@
-"""GPU parity of the dense attention for full steps (ec_dense_attention: SM pairs, 2-CTA
-tensor-core products) against the float64 oracle.
+"""GPU parity of the dense attention for full steps (ec_dense_attention: two query tiles per
+CTA, one softmax warpgroup per tile) against the float64 oracle.
 
 Tolerance as for the partial attention (bf16 outputs): per head ||O - O_ref||_F <= 2e-2
 ||O_ref||_F and per element |O - O_ref| <= 2e-2 (|O_ref| + rms(O_ref)). Every row must be
 written. Cases: the LLaDA-8B layer (MHA 32 x 128, L 1024) on sampled rows, grouped queries with
-a ragged key block and an odd tile count (the last pair's second CTA idle), several sequences,
-a tile count that needs several items per cluster, a single ragged block, and a sharp softmax
+a ragged key block and an odd tile count (the last item's second tile past the end), several
+sequences, a tile count that needs several items per CTA, a single ragged block, and a sharp softmax
 (the lazy rescale).
 """
 import math
@@ -71,8 +71,8 @@ def test_llada_layer_shape(E):
 
 
 def test_gqa_ragged_block_odd_tiles(E):
-    # g = 7: 18 positions per tile, ceil(520 / 18) = 29 tiles per head (the last pair's second
-    # CTA has no tile); 520 = 4 * 128 + 8 keys (a ragged last block)
+    # g = 7: 18 positions per tile, ceil(520 / 18) = 29 tiles per head (the last item's second
+    # tile lies past the end); 520 = 4 * 128 + 8 keys (a ragged last block)
     run_dense(E, B=2, L=520, Hq=28, Hkv=4, seed=2)
 
 
@@ -80,8 +80,9 @@ def test_mha_odd_tiles_three_sequences(E):
     run_dense(E, B=3, L=384, Hq=2, Hkv=2, seed=3)
 
 
-def test_many_items_per_cluster(E):
-    # 4 sequences x 8 heads x 8 pairs = 256 pair items: more than the clusters that fit at once
+def test_many_items_per_cta(E):
+    # 4 sequences x 8 heads x 8 tile pairs = 256 items: more than one per SM, so CTAs take
+    # several items (the Q, S and O buffers are reused across items)
     run_dense(E, B=4, L=2048, Hq=8, Hkv=8, seed=4, rows=tile_edges(2048, 128, step=11))
 
 

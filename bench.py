@@ -1043,6 +1043,9 @@ def emit_ours(args, res, rank, world):
         fa = cfg["llada_layer_full"]["partial_attention"]
         targets["attention_bf16"] = {"kernel": "partial_attention", "workload": "llada_layer, full step (R = L)",
                                      "frac": fa["frac_bf16"], "goal": 0.50, "of": "measured bf16 dense (cuBLAS burst)"}
+        da = cfg["llada_layer_full"].get("dense_attention")
+        if da:  # the kernel for steps known to be full, on the same step
+            targets["attention_bf16"]["dense_attention_frac"] = da["frac_bf16"]
     if "dream_gqa" in cfg:
         targets["entropy_decode_hbm_dream"] = {"kernel": "entropy_decode", "workload": "dream_gqa (78 MB)",
                                                "frac": cfg["dream_gqa"]["entropy_decode"]["frac_hbm"],

@@ -123,6 +123,15 @@ def test_long_context_step(E):
     run_and_check(E, w, W.snapshot_state(w), W.step_logits(w), W.layer_tensors(w, 0), sample_rows=32)
 
 
+@pytest.mark.parametrize("cfg,scale", [(2, {}), (3, dict(B=2, L=512, prompt=256, gen=256, V=32000, seed=23))])
+def test_always_full_step(E, cfg, scale):
+    # tau < 0: every entropy (0 for an empty decode set) exceeds it, so every step is full and,
+    # with no scope, ec_step runs the attention on the two-tile dense kernel (MHA and GQA)
+    w = W.workload(cfg).scaled(tau=-1.0, **scale)
+    flags = run_and_check(E, w, W.snapshot_state(w), W.step_logits(w), W.layer_tensors(w, 0), sample_rows=64)
+    assert all(flags)
+
+
 def test_mixed_flags_in_one_batch(E):
     # Dream-7B-shaped heads, four sequences: even ones commit a near-certain token (partial
     # step), odd ones a near-uniform one (full step).

@@ -264,7 +264,8 @@ def partial_attention(p: Params, q, k_cache, v_cache, R, out, scale: float | Non
 
 def dense_attention(p: Params, q, k_cache, v_cache, out, scale: float | None = None, dev_err=None, stream=None):
     """(d) for a step known to be full: out[b, r, h] = softmax(scale q k^T) v over all L keys for
-    every position r (q in position order), on SM pairs with 2-CTA products; D = 128."""
+    every position r (q in position order), two query tiles per CTA with a softmax warpgroup
+    each; D = 128."""
     pc = p.c()
     sc = (1.0 / math.sqrt(p.D)) if scale is None else float(scale)
     st = lib().ec_dense_attention(ctypes.byref(pc), _vp(q), _vp(k_cache), _vp(v_cache), sc, _vp(out), _vp(dev_err),

@@ -118,7 +118,7 @@ def test_dense_attention_rejects_bad_args(capi):
     good = _params(capi, D=128)
     for bad, want in [
         (_params(capi, D=128, Hkv=5), capi.EC_ERR_INVALID_ARG),  # Hq % Hkv
-        (_params(capi, D=64), capi.EC_ERR_UNSUPPORTED),  # the pair kernel splits V's 128 dims
+        (_params(capi, D=64), capi.EC_ERR_UNSUPPORTED),  # the dense kernel is built for D = 128
         (_params(capi, D=96), capi.EC_ERR_UNSUPPORTED),
         (_params(capi, D=128, B=0), capi.EC_ERR_INVALID_ARG),
         (_params(capi, D=128, L=0), capi.EC_ERR_INVALID_ARG),

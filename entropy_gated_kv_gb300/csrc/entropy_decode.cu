@@ -46,7 +46,7 @@ constexpr int kWideVec = 8;     // the cluster launch's double-width pieces
 constexpr bool kSplitScalar = false;
 constexpr bool kWideScalar = true;
 constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
-constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs
+constexpr int kClusterCtasPerSm = 2;  // cluster path while rows x cluster <= this x SMs (all resident)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DT>
@@ -369,15 +369,40 @@ __global__ void __launch_bounds__(kThreads) entropy_split_kernel(EntArgs a) {
   publish_chunk(a, row, chunk, p, has, wpart);
 }
 
+// Waits for the first phase of a barrier that other CTAs of the cluster complete with remote
+// stores (acquire at cluster scope: their data is visible once it returns true). Gives up after
+// kLandedWaitNs of wall time (the stores are issued right after a cluster barrier, so this
+// never binds unless the hardware misbehaves).
+constexpr uint64_t kLandedWaitNs = 1000000000ull;
+__device__ __forceinline__ bool wait_landed(uint64_t* bar) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar))
+        : "memory");
+    if (done) return true;
+    if ((i & 63u) == 63u && global_timer_ns() - t0 > kLandedWaitNs) return false;
+  }
+}
+
 // Cluster path: one cluster per row; CTA `rank` of the cluster takes a contiguous run of the
 // row's double-width pieces (8 vectors per lane, 2048 bf16 elements), its warps take every
 // 8th piece of the run (at the sizes it serves, one piece each, all loads in flight at once),
-// the 8 warps merge in shared memory and the cluster's first CTA merges the CTAs through
-// distributed shared memory and writes the row result.
+// and the 8 warps merge in shared memory. Each other CTA then pushes its 16-byte partial into
+// the first CTA's shared memory with one asynchronous remote store, counted on the first CTA's
+// barrier, and exits; the first CTA merges the cluster's partials and writes the row. The one
+// cluster barrier (which publishes the first CTA's barrier before any store into it) is
+// arrived at on entry and waited on only before the store, so it overlaps the loads.
 template <int DT>
-__global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) entropy_cluster_kernel(EntArgs a) {
   __shared__ __align__(16) Part wpart[kWarps];
-  __shared__ __align__(16) Part slice;
+  __shared__ __align__(16) Part slices[kMaxCluster];  // the first CTA: one partial per CTA of the cluster
+  __shared__ __align__(8) uint64_t landed;            // the first CTA: the other CTAs' partials are in
   pdl_wait();  // logits and row counts may come from the previous kernel in the stream
   pdl_launch_dependents();
   const int csize = static_cast<int>(cluster_size());
@@ -385,6 +410,11 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
   const int row = static_cast<int>(cluster_id_x());
   if (row_skipped(a, row)) return;  // the whole cluster skips the row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (rank == 0 && threadIdx.x == 0) {
+    mbar_init(&landed, 1);
+    fence_mbar_init();
+  }
+  cluster_arrive_release();
   const char* rowp = a.logits + static_cast<int64_t>(row) * a.row_stride_bytes;
   constexpr int LV = kWideVec;
   constexpr int PE = piece_elems<DT, LV>();
@@ -399,32 +429,46 @@ __global__ void __launch_bounds__(kThreads) entropy_cluster_kernel(EntArgs a) {
   }
   if (lane == 0) wpart[warp] = acc;
   __syncthreads();
-  if (warp == 0) {
-    Part p = lane < kWarps ? wpart[lane] : Part{-INFINITY, INT_MAX, 0.f, 0.f};
+  cluster_wait_acquire();  // the first CTA's barrier is initialised
+  if (warp != 0) return;
+  Part p = lane < kWarps ? wpart[lane] : Part{-INFINITY, INT_MAX, 0.f, 0.f};
 #pragma unroll
-    for (int off = 1; off < kWarps; off <<= 1) {
-      const Part o{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.i, off),
-                   __shfl_xor_sync(0xffffffffu, p.s, off), __shfl_xor_sync(0xffffffffu, p.t, off)};
-      ent_part_merge(p, o);
-    }
-    if (lane == 0) slice = p;
+  for (int off = 1; off < kWarps; off <<= 1) {
+    const Part o{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.i, off),
+                 __shfl_xor_sync(0xffffffffu, p.s, off), __shfl_xor_sync(0xffffffffu, p.t, off)};
+    ent_part_merge(p, o);
   }
-  cluster_sync_all();  // every slice result is in its CTA's shared memory
-  if (rank == 0 && warp == 0) {
-    Part p{-INFINITY, INT_MAX, 0.f, 0.f};
-    if (lane < csize) {
-      const float4 q = dsmem_ld_f4(dsmem_map(smem_u32(&slice), static_cast<uint32_t>(lane)));
-      p = Part{q.x, __float_as_int(q.y), q.z, q.w};
+  if (rank != 0) {
+    if (lane == 0)
+      st_async_v4(dsmem_map(smem_u32(&slices[rank]), 0u),
+                  make_uint4(__float_as_uint(p.m), static_cast<uint32_t>(p.i), __float_as_uint(p.s),
+                             __float_as_uint(p.t)),
+                  dsmem_map(smem_u32(&landed), 0u));
+    return;
+  }
+  if (lane == 0) {
+    slices[0] = p;
+    mbar_arrive_expect_tx(&landed, static_cast<uint32_t>(csize - 1) * 16u);
+  }
+  __syncwarp();
+  if (!__all_sync(0xffffffffu, wait_landed(&landed))) {
+    // a partial never arrived: mark the row (the decode entries carry no error word)
+    if (lane == 0) {
+      a.ids[row] = -1;
+      a.entropy[row] = __int_as_float(0x7FC00000);
+      a.log_conf[row] = __int_as_float(0x7FC00000);
     }
+    return;
+  }
+  Part q = Part{-INFINITY, INT_MAX, 0.f, 0.f};
+  if (lane < csize) q = slices[lane];
 #pragma unroll
-    for (int off = 1; off < kMaxCluster; off <<= 1) {
-      const Part o{__shfl_xor_sync(0xffffffffu, p.m, off), __shfl_xor_sync(0xffffffffu, p.i, off),
-                   __shfl_xor_sync(0xffffffffu, p.s, off), __shfl_xor_sync(0xffffffffu, p.t, off)};
-      ent_part_merge(p, o);
-    }
-    if (lane == 0) write_row(row, p, a.ids, a.entropy, a.log_conf);
+  for (int off = 1; off < kMaxCluster; off <<= 1) {
+    const Part o{__shfl_xor_sync(0xffffffffu, q.m, off), __shfl_xor_sync(0xffffffffu, q.i, off),
+                 __shfl_xor_sync(0xffffffffu, q.s, off), __shfl_xor_sync(0xffffffffu, q.t, off)};
+    ent_part_merge(q, o);
   }
-  cluster_sync_all();  // peers keep their shared memory until it has been read
+  if (lane == 0) write_row(row, q, a.ids, a.entropy, a.log_conf);
 }
 
 // Merges each row's chunk partials (one warp per row) and writes the row's results.

@@ -349,11 +349,13 @@ __device__ __forceinline__ void publish_chunk(const EntArgs& a, int row, int chu
 }
 
 // Split path: CTA (row, c) takes chunk c of the row (pieces 8 c .. 8 c + 7, one per warp, of
-// LV vectors per lane). The standalone launch (kAloneVec pieces, many rows) keeps 6 CTAs per SM
-// resident (40 registers): more loads in flight per SM measured faster at 78 MB (18.9 ->
-// 18.1 us).
+// LV vectors per lane). Every instantiation is held to 6 resident CTAs per SM (at most 40
+// registers). For the standalone launch (kAloneVec pieces, many rows) that keeps more loads in
+// flight per SM (measured faster at 78 MB: 18.9 -> 18.1 us); the step's 4-vector pieces need no
+// more than that anyway (39 registers unbounded; a bound of 1 CTA let them grow to 67 and slowed
+// the step).
 template <int DT, int LV>
-__global__ void __launch_bounds__(kThreads, LV == kAloneVec ? 6 : 1) entropy_split_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) entropy_split_kernel(EntArgs a) {
   __shared__ Part wpart[kWarps];
   pdl_wait();  // logits and row counts may come from the previous kernel in the stream
   pdl_launch_dependents();

@@ -46,7 +46,7 @@ constexpr int kWideVec = 8;     // the cluster launch's double-width pieces
 constexpr bool kSplitScalar = false;
 constexpr bool kWideScalar = true;
 constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
-constexpr int kClusterCtasPerSm = 2;  // cluster path while rows x cluster <= this x SMs (all resident)
+constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs (all resident)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DT>
@@ -401,9 +401,10 @@ __device__ __forceinline__ bool wait_landed(uint64_t* bar) {
 // the first CTA's shared memory with one asynchronous remote store, counted on the first CTA's
 // barrier, and exits; the first CTA merges the cluster's partials and writes the row. The one
 // cluster barrier (which publishes the first CTA's barrier before any store into it) is
-// arrived at on entry and waited on only before the store, so it overlaps the loads.
+// arrived at on entry and waited on only before the store, so it overlaps the loads. Held to 4
+// CTAs per SM (64 registers): measured faster than 2 (127) or 3 (79) at 32 rows of 126464.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) entropy_cluster_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) entropy_cluster_kernel(EntArgs a) {
   __shared__ __align__(16) Part wpart[kWarps];
   __shared__ __align__(16) Part slices[kMaxCluster];  // the first CTA: one partial per CTA of the cluster
   __shared__ __align__(8) uint64_t landed;            // the first CTA: the other CTAs' partials are in

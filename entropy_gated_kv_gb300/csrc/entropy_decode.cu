@@ -46,7 +46,8 @@ constexpr int kWideVec = 8;     // the cluster launch's double-width pieces
 constexpr bool kSplitScalar = false;
 constexpr bool kWideScalar = true;
 constexpr int kMaxCluster = 8;  // CTAs per row (portable cluster size)
-constexpr int kClusterCtasPerSm = 4;  // cluster path while rows x cluster <= this x SMs (all resident)
+constexpr int kClusterCtasPerSmBf16 = 4;  // cluster path while rows x cluster <= this x SMs (all resident;
+constexpr int kClusterCtasPerSmF32 = 2;   // the cluster kernel's launch bounds per type)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DT>
@@ -401,10 +402,11 @@ __device__ __forceinline__ bool wait_landed(uint64_t* bar) {
 // the first CTA's shared memory with one asynchronous remote store, counted on the first CTA's
 // barrier, and exits; the first CTA merges the cluster's partials and writes the row. The one
 // cluster barrier (which publishes the first CTA's barrier before any store into it) is
-// arrived at on entry and waited on only before the store, so it overlaps the loads. Held to 4
-// CTAs per SM (64 registers): measured faster than 2 (127) or 3 (79) at 32 rows of 126464.
+// arrived at on entry and waited on only before the store, so it overlaps the loads. bf16 is
+// held to 4 CTAs per SM (64 registers): measured faster than 2 (127) or 3 (79) at 32 rows of
+// 126464. fp32 keeps 2 (at 64 registers it spills, and the 32-row fp32 decode slowed).
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) entropy_cluster_kernel(EntArgs a) {
+__global__ void __launch_bounds__(kThreads, DT == EC_BF16 ? 4 : 2) entropy_cluster_kernel(EntArgs a) {
   __shared__ __align__(16) Part wpart[kWarps];
   __shared__ __align__(16) Part slices[kMaxCluster];  // the first CTA: one partial per CTA of the cluster
   __shared__ __align__(8) uint64_t landed;            // the first CTA: the other CTAs' partials are in
@@ -520,7 +522,8 @@ cudaError_t launch_entropy_decode(const void* logits, int64_t row_stride, int32_
   const int64_t wide = kWarps * (f32 ? piece_elems<EC_F32, kWideVec>() : piece_elems<EC_BF16, kWideVec>());
   const int csize = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxCluster, (V + wide - 1) / wide)));
   const int64_t cluster_ctas = static_cast<int64_t>(n_rows) * csize;
-  if (!publish_only && (ws == nullptr || (allow_cluster && cluster_ctas <= static_cast<int64_t>(kClusterCtasPerSm) * sms))) {
+  const int per_sm = f32 ? kClusterCtasPerSmF32 : kClusterCtasPerSmBf16;
+  if (!publish_only && (ws == nullptr || (allow_cluster && cluster_ctas <= static_cast<int64_t>(per_sm) * sms))) {
     // few rows, or no workspace: merge on chip, write the rows
     if (cluster_ctas > INT_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(cluster_ctas));

@@ -183,16 +183,16 @@ __global__ void __maxnreg__(kMaxRegs) dense_tiles_kernel(
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Per item: S of sub-blocks 0 and 1 for both tiles, then per sub-block s and tile t:
-    // PV_t(s), then S_t(s + 2) into the buffer PV_t(s) has just released.
+    // Per item: both tiles' S of the first block, then per block and tile t: PV_t of the block,
+    // then S_t of the next block into the buffer that PV_t has just released.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kSubN, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, 1);
       const uint32_t q_lo0 = sdesc_lo(smem_u32(q_smem), 16);
       const uint32_t q_lo1 = sdesc_lo(smem_u32(q_smem + kQBytes), 16);
-      uint32_t it = 0;  // K/V blocks consumed so far (sub-block counter = 2 it + s)
+      uint32_t it = 0;  // K/V blocks consumed so far
       bool ok = true;
-      // S_t(s) = Q_t K(s)^T into tile t's buffer s % 2; K block `kb` is in stage kb % kStages.
+      // S_t = Q_t K^T for sub-block h of K/V block kb (in stage kb % kStages) into tile t's buffer h.
       auto issue_qk = [&](int t, uint32_t kb, int h) {
         const uint32_t k_lo = sdesc_lo(smem_u32(stage0 + (kb % kStages) * kStageBytes + h * kSubK), 16);
         const uint32_t s_col = tmem + (t * kNBuf + h) * kSubN;

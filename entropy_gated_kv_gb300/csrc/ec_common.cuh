@@ -263,13 +263,6 @@ EC_DEV uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// Remote loads are volatile (kept in program order after the cluster barrier) but carry no
-// memory clobber, so a run of them is issued back to back.
-EC_DEV float4 dsmem_ld_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-  return v;
-}
 // Stores 16 bytes into another CTA's shared memory (remote_addr from dsmem_map) and counts
 // them on that CTA's mbarrier (remote_bar from dsmem_map) as completed transaction bytes.
 EC_DEV void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
@@ -277,11 +270,6 @@ EC_DEV void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
                    remote_addr),
                "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
                : "memory");
-}
-EC_DEV float dsmem_ld_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
 }
 
 }  // namespace ec
@@ -300,23 +288,6 @@ EC_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_depend
 }  // namespace ec
 
 namespace ec {
-
-// Bulk copy from global memory to this CTA's shared memory (the async copy engine, no tensor
-// map); completion is counted in bytes on `bar`. Both addresses 16-byte aligned, size a
-// multiple of 16. evict_first: the source is read once, so it should leave L2 first.
-EC_DEV void bulk_load_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t l2_policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(l2_policy)
-      : "memory");
-}
-
-EC_DEV uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 
 // Bulk copy from this CTA's shared memory to (possibly another CTA's) shared memory in the
 // cluster; completion is counted in bytes on the destination's mbarrier. Addresses 16-byte

@@ -5,7 +5,8 @@ Tolerance as for the partial attention (bf16 outputs): per head ||O - O_ref||_F 
 ||O_ref||_F and per element |O - O_ref| <= 2e-2 (|O_ref| + rms(O_ref)). Every row must be
 written. Cases: the LLaDA-8B layer (MHA 32 x 128, L 1024) on sampled rows, grouped queries with
 a ragged key block and an odd tile count (the last item's second tile past the end), several
-sequences, a tile count that needs several items per CTA, a single ragged block, and a sharp softmax
+sequences, a tile count that needs several items per CTA, a single ragged block, a single
+position, 16 query heads per KV head (8 positions per tile), and a sharp softmax
 (the lazy rescale).
 """
 import math
@@ -88,6 +89,19 @@ def test_many_items_per_cta(E):
 
 def test_single_ragged_block(E):
     run_dense(E, B=1, L=100, Hq=8, Hkv=2, seed=5)
+
+
+def test_single_position(E):
+    # L = 1: one item whose first tile holds one row and whose second tile is past the end; one
+    # key, so every output row is that key's V row
+    got = run_dense(E, B=2, L=1, Hq=4, Hkv=2, seed=8)
+    assert got.shape == (2, 1, 4, 128)
+
+
+def test_sixteen_query_heads_per_kv_head(E):
+    # g = 16 packs 8 positions per tile; L = 37 gives 5 tiles (3 items, the last one half empty)
+    # and a single ragged key block
+    run_dense(E, B=2, L=37, Hq=32, Hkv=2, seed=9)
 
 
 def test_sharp_softmax_rescale(E):

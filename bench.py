@@ -676,11 +676,19 @@ def layer_setup(E, dev):
     return p, lw, x_src, kc, vc, st.idx, st.R, dff, w
 
 
+def full_step_pattern(n, rate):
+    """Which of n steps are full when a fraction `rate` of them is: round(rate * n) full steps
+    spread evenly over the n (step i is full when floor((i + 1) * m / n) > floor(i * m / n))."""
+    m = round(rate * n)
+    return [(i + 1) * m // n > i * m // n for i in range(n)]
+
+
 def run_layer_forward(E, dev, n_steps) -> dict:
     """The partial forward of one LLaDA-8B-shaped layer for the headline step's recompute set
     (R = 95), against the full forward (R = L): the time per layer of the forward each flag
     selects, and its roofline (weight bytes for the partial forward, tensor-core flops for the
-    full one). Graph-replayed."""
+    full one). Then the time per layer over a run of steps in which a given fraction are full
+    (the flag rate), against a run of full steps only. Graph-replayed."""
     import torch
 
     p, lw, x_src, kc, vc, idx_p, R_p, dff, w = layer_setup(E, dev)
@@ -689,20 +697,30 @@ def run_layer_forward(E, dev, n_steps) -> dict:
     y = torch.empty(1, L, d, dtype=bf, device=dev)
     out = {}
     full_idx = torch.arange(L, dtype=torch.int32, device=dev).view(1, L)
-    for name, idx, R in (("partial", idx_p, R_p), ("full", full_idx, torch.tensor([L], dtype=torch.int32, device=dev))):
-        n = n_steps if name == "partial" else max(10, n_steps // 8)
-        E.layer_forward(p, lw, idx, R, x_src, kc, vc, y=y, ws=ws)
+    R_full = torch.tensor([L], dtype=torch.int32, device=dev)
+
+    def time_run(pattern):
+        """Mean time per layer forward over one graph of the pattern's steps (True = full)."""
+        for full in sorted(set(pattern)):
+            E.layer_forward(p, lw, full_idx if full else idx_p, R_full if full else R_p, x_src, kc, vc, y=y, ws=ws)
         torch.cuda.synchronize()
         gr = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream(device=dev)
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(gr, stream=s):
-                for _ in range(n):
-                    E.layer_forward(p, lw, idx, R, x_src, kc, vc, y=y, ws=ws)
+                for full in pattern:
+                    E.layer_forward(p, lw, full_idx if full else idx_p, R_full if full else R_p, x_src, kc, vc,
+                                    y=y, ws=ws)
         torch.cuda.current_stream().wait_stream(s)
         warm_replay(gr, 50.0)
-        us = statistics.median(replay_ms([gr], dev) for _ in range(3)) * 1e3 / n
+        us = statistics.median(replay_ms([gr], dev) for _ in range(3)) * 1e3 / len(pattern)
+        del gr
+        return us
+
+    for name, idx, R in (("partial", idx_p, R_p), ("full", full_idx, R_full)):
+        n = n_steps if name == "partial" else max(10, n_steps // 8)
+        us = time_run([name == "full"] * n)
         rows = int(R.sum().item())
         params = d * (d + 2 * w.Hkv * w.D) + d * d + 3 * d * dff
         wbytes = 2 * params
@@ -710,8 +728,17 @@ def run_layer_forward(E, dev, n_steps) -> dict:
         pk = peaks()
         out[name] = {"R": rows, "us": us, "weight_GB/s": wbytes / (us * 1e3), "TFLOP/s": flops / (us * 1e6),
                      "frac_hbm": wbytes / (us * 1e3) / pk["hbm_gbs"], "frac_bf16": flops / (us * 1e6) / pk["bf16_tflops"]}
-        del gr
     out["full_over_partial"] = out["full"]["us"] / out["partial"]["us"]
+    n_mix = 40
+    by_rate = {}
+    for rate in (0.0, 0.1, 0.25, 0.5, 1.0):
+        us = time_run(full_step_pattern(n_mix, rate))
+        by_rate[f"{rate:g}"] = {"us_per_layer": us, "speedup_vs_all_full": None}
+    for v in by_rate.values():
+        v["speedup_vs_all_full"] = by_rate["1"]["us_per_layer"] / v["us_per_layer"]
+    out["by_flag_rate"] = by_rate
+    out["by_flag_rate_run"] = (f"{n_mix} layer forwards per graph, the given fraction of them full (R = L) and spread "
+                               f"evenly, the rest partial (R = {int(R_p.sum().item())})")
     out["workload"] = (f"one LLaDA-8B-shaped layer: d {d}, {w.Hq} x {w.D} MHA, d_ff {dff}, L {L}; RMSNorm, QKV + RoPE, "
                        f"K/V refresh, attention, O-proj + residual, RMSNorm, SwiGLU, down + residual")
     out["weights_MB"] = 2 * (d * (d + 2 * w.Hkv * w.D) + d * d + 3 * d * dff) / 1e6

@@ -145,3 +145,16 @@ def test_config_entry_against_its_binding_roofline():
     e = bench.summarise_config(w, 40000.0, 0, 95, kern, 50e6, "host")  # partial: 87 flops per byte
     assert e["partial_attention"]["bound"] == "hbm"
     assert e["partial_attention"]["frac_bound"] == pytest.approx(e["partial_attention"]["frac_hbm"])
+
+
+@pytest.mark.parametrize("n,rate", [(40, 0.0), (40, 0.1), (40, 0.25), (40, 0.5), (40, 1.0), (7, 0.3), (1, 1.0)])
+def test_full_step_pattern(n, rate):
+    """The flag-rate runs of the layer forward: round(rate * n) full steps, spread so that every
+    window of n / m consecutive steps holds one of them."""
+    p = bench.full_step_pattern(n, rate)
+    m = round(rate * n)
+    assert len(p) == n and sum(p) == m
+    if 0 < m < n:
+        where = [i for i, f in enumerate(p) if f]
+        gaps = {b - a for a, b in zip(where, where[1:])}
+        assert max(gaps) - min(gaps) <= 1

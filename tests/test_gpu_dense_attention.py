@@ -3,7 +3,8 @@ CTA, one softmax warpgroup per tile) against the float64 oracle.
 
 Tolerance as for the partial attention (bf16 outputs): per head ||O - O_ref||_F <= 2e-2
 ||O_ref||_F and per element |O - O_ref| <= 2e-2 (|O_ref| + rms(O_ref)). Every row must be
-written. Cases: the LLaDA-8B layer (MHA 32 x 128, L 1024) on sampled rows, grouped queries with
+written. Cases: the LLaDA-8B layer (MHA 32 x 128, L 1024) and the Dream-7B batch (B 8, GQA
+28 / 4 x 128, L 2048, the shape the bench times) on sampled rows, grouped queries with
 a ragged key block and an odd tile count (the last item's second tile past the end), several
 sequences, a tile count that needs several items per CTA, a single ragged block, a single
 position, 16 query heads per KV head (8 positions per tile), and a sharp softmax
@@ -69,6 +70,12 @@ def tile_edges(L, nr, step=7):
 
 def test_llada_layer_shape(E):
     run_dense(E, B=1, L=1024, Hq=32, Hkv=32, seed=1, rows=tile_edges(1024, 128))
+
+
+def test_dream_batch_shape(E):
+    # g = 7: 18 positions per tile, 114 tiles per (sequence, KV head), 57 items each, 1824 items
+    # over the persistent CTAs
+    run_dense(E, B=8, L=2048, Hq=28, Hkv=4, seed=10, rows=tile_edges(2048, 128 // 7, step=13))
 
 
 def test_gqa_ragged_block_odd_tiles(E):

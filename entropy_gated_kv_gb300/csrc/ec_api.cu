@@ -397,16 +397,17 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
   if (e != cudaSuccess) return EC_ERR_CUDA;
   // Entropies are non-negative (an empty decode set counts 0, a NaN counts as full), so with
   // tau < 0 the gate fires on every step. Without a scope every step then recomputes every
-  // position in order, and the attention is the dense one for every sequence: the two-tile
-  // kernel runs it on the gathered queries.
+  // position in order (idx is the identity), and the attention is the dense one for every
+  // sequence: the two-tile kernel reads the position-indexed queries where they are, and the
+  // scatter kernel refreshes the cache only (no query gather).
   const bool always_full = p->tau < 0.f && !has_scope(*p) && p->D == 128;
   for (int32_t l = 0; l < n_layers; ++l) {
-    e = launch_kv_scatter(*p, k_cache[l], v_cache[l], k_src[l], v_src[l], 1, st->idx, st->R, q_src[l],
-                          w + lay.qbuf, st->dev_err, s);
+    e = launch_kv_scatter(*p, k_cache[l], v_cache[l], k_src[l], v_src[l], 1, st->idx, st->R,
+                          always_full ? nullptr : q_src[l], always_full ? nullptr : w + lay.qbuf, st->dev_err, s);
     if (e != cudaSuccess) return EC_ERR_CUDA;
     ec_status as = EC_OK;
     if (always_full)
-      launch_dense_attention_tiles(*p, w + lay.qbuf, k_cache[l], v_cache[l], scale, out[l], st->dev_err, s, &as);
+      launch_dense_attention_tiles(*p, q_src[l], k_cache[l], v_cache[l], scale, out[l], st->dev_err, s, &as);
     else
       launch_partial_attention(*p, w + lay.qbuf, k_cache[l], v_cache[l], st->R, scale, out[l], w + lay.attn,
                                st->dev_err, true, s, &as);

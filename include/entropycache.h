@@ -398,8 +398,9 @@ ec_status ec_rope_table(int32_t L, int32_t D, float theta, float* rope_cos, floa
  * cand_pos, cand_count: as for ec_select_recompute.
  * ws at least ec_step_workspace_size(p) bytes (16-byte aligned, no initial contents needed).
  * scale as for ec_partial_attention. With tau < 0, no scope and D = 128 every step is full
- * (entropies are non-negative), so the attention runs on the kernel of ec_dense_attention;
- * otherwise on the kernel of ec_partial_attention. */
+ * (entropies are non-negative), so the attention runs on the kernel of ec_dense_attention,
+ * reading q_src[l] in place (the recompute order is the position order); otherwise on the
+ * kernel of ec_partial_attention, from the gathered queries. */
 size_t ec_step_workspace_size(const ec_params* p);
 ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits,
                   const int32_t* cand_pos, const int32_t* cand_count, int32_t n_layers,

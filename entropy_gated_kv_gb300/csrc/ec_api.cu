@@ -73,6 +73,27 @@ constexpr int32_t kMaxCmax = 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The byte ranges [a, a + na) and [b, b + nb) share a byte (addresses compared, never read).
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+size_t q_bytes(const ec_params& p) { return static_cast<size_t>(p.B) * p.L * p.Hq * p.D * 2; }
+size_t kv_bytes(const ec_params& p) { return static_cast<size_t>(p.B) * p.L * p.Hkv * p.D * 2; }
+
+// The attention writes out ([B, L, Hq, D]) while it reads q, k_cache and v_cache.
+bool attention_io_overlap(const ec_params& p, const void* q, const void* k, const void* v, const void* out) {
+  const size_t nq = q_bytes(p), nkv = kv_bytes(p);
+  return overlaps(out, nq, q, nq) || overlaps(out, nq, k, nkv) || overlaps(out, nq, v, nkv);
+}
+
+// The scatter writes both caches while it reads the fresh rows ([B, L, Hkv, D] each).
+bool scatter_io_overlap(const ec_params& p, const void* kc, const void* vc, const void* kn, const void* vn) {
+  const size_t n = kv_bytes(p);
+  return overlaps(kc, n, vc, n) || overlaps(kc, n, kn, n) || overlaps(kc, n, vn, n) || overlaps(vc, n, kn, n) ||
+         overlaps(vc, n, vn, n);
+}
+
 ec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? EC_OK : EC_ERR_CUDA; }
 
 // Shape checks common to the stages that need them. `what` selects the groups checked.
@@ -264,6 +285,7 @@ ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const 
   if (!k_cache || !v_cache || !k_new || !v_new || !idx || !R) return EC_ERR_INVALID_ARG;
   if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
     return EC_ERR_INVALID_ARG;
+  if (scatter_io_overlap(*p, k_cache, v_cache, k_new, v_new)) return EC_ERR_INVALID_ARG;
   return cuda_status(launch_kv_scatter(*p, k_cache, v_cache, k_new, v_new, src_by_position, idx, R, nullptr,
                                        nullptr, dev_err, static_cast<cudaStream_t>(stream)));
 }
@@ -282,6 +304,7 @@ ec_status ec_dense_attention(const ec_params* p, const void* q, const void* k_ca
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return EC_ERR_INVALID_ARG;
   if (!(scale == scale)) return EC_ERR_INVALID_ARG;
   if (p->D != 128) return EC_ERR_UNSUPPORTED;
+  if (attention_io_overlap(*p, q, k_cache, v_cache, out)) return EC_ERR_INVALID_ARG;
   ec_status st = EC_OK;
   launch_dense_attention_tiles(*p, q, k_cache, v_cache, scale, out, dev_err, static_cast<cudaStream_t>(stream), &st);
   return st;
@@ -297,6 +320,7 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
     return EC_ERR_INVALID_ARG;
   if (ws_bytes < attention_workspace_bytes(*p)) return EC_ERR_INVALID_ARG;
   if (!(scale == scale)) return EC_ERR_INVALID_ARG;
+  if (attention_io_overlap(*p, q, k_cache, v_cache, out)) return EC_ERR_INVALID_ARG;
   ec_status st = EC_OK;
   launch_partial_attention(*p, q, k_cache, v_cache, R, scale, out, ws, dev_err, false, static_cast<cudaStream_t>(stream),
                            &st);
@@ -375,6 +399,9 @@ ec_status ec_step(const ec_params* p, const ec_state* st, const void* logits, co
     if (!k_cache[l] || !v_cache[l] || !k_src[l] || !v_src[l] || !q_src[l] || !out[l]) return EC_ERR_INVALID_ARG;
     if (!aligned16(k_cache[l]) || !aligned16(v_cache[l]) || !aligned16(k_src[l]) || !aligned16(v_src[l]) ||
         !aligned16(q_src[l]) || !aligned16(out[l]))
+      return EC_ERR_INVALID_ARG;
+    if (scatter_io_overlap(*p, k_cache[l], v_cache[l], k_src[l], v_src[l]) ||
+        attention_io_overlap(*p, q_src[l], k_cache[l], v_cache[l], out[l]))
       return EC_ERR_INVALID_ARG;
   }
   const StepLayout lay = step_layout(*p);

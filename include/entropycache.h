@@ -298,7 +298,8 @@ ec_status ec_candidates(const ec_params* p, const ec_state* st, int32_t mode, in
  * k_cache, v_cache  bf16 [B, L, Hkv, D]; k_new, v_new bf16 [B, L, Hkv, D].
  * idx int32 [B, L], R int32 [B] on the device. An idx outside [0, L) sets
  * EC_DEVERR_BAD_IDX and that row is skipped; R outside [0, L] sets EC_DEVERR_BAD_R and
- * that sequence is skipped. k_new/v_new must not overlap the caches. */
+ * that sequence is skipped. k_new/v_new must not overlap the caches, nor the two caches
+ * each other (checked on the host over the [B, L, Hkv, D] extents: EC_ERR_INVALID_ARG). */
 ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const void* k_new,
                         const void* v_new, int32_t src_by_position, const int32_t* idx,
                         const int32_t* R, int32_t* dev_err, ec_stream_t stream);
@@ -319,7 +320,9 @@ ec_status ec_kv_scatter(const ec_params* p, void* k_cache, void* v_cache, const 
  *         merge runs in on-chip shared memory of a 4-CTA cluster).
  * Products run on bf16 tensor cores with fp32 accumulation; probabilities are rounded to
  * bf16 before the PV product. A pipeline wait that exceeds its limit sets
- * EC_DEVERR_TIMEOUT in dev_err (if given) and leaves that tile unwritten. */
+ * EC_DEVERR_TIMEOUT in dev_err (if given) and leaves that tile unwritten. out must not
+ * overlap q, k_cache or v_cache (checked on the host over the extents above:
+ * EC_ERR_INVALID_ARG). */
 size_t ec_partial_attention_workspace_size(const ec_params* p);
 ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* R, float scale, void* out,
@@ -336,7 +339,8 @@ ec_status ec_partial_attention(const ec_params* p, const void* q, const void* k_
  *   out[b, r, h, :] = sum_j softmax_j(scale * <q[b, r, h, :], k_cache[b, j, h/g, :]>) v_cache[b, j, h/g, :]
  * q, out bf16 [B, L, Hq, D]; k_cache, v_cache bf16 [B, L, Hkv, D]; D = 128 (other head
  * sizes return EC_ERR_UNSUPPORTED). No workspace. Rounding as ec_partial_attention. A
- * pipeline wait that exceeds its limit sets EC_DEVERR_TIMEOUT in dev_err (if given). */
+ * pipeline wait that exceeds its limit sets EC_DEVERR_TIMEOUT in dev_err (if given). out
+ * must not overlap q, k_cache or v_cache (EC_ERR_INVALID_ARG). */
 ec_status ec_dense_attention(const ec_params* p, const void* q, const void* k_cache, const void* v_cache,
                              float scale, void* out, int32_t* dev_err, ec_stream_t stream);
 
@@ -394,7 +398,9 @@ ec_status ec_rope_table(int32_t L, int32_t D, float theta, float* rope_cos, floa
  * order). One flag and one recompute set serve every layer (zh summary §2.3: the decision
  * is independent of depth). The flag computed from this step's logits governs this
  * call's attention stage, which stands for the next forward pass of the workflow.
- * The pointer arrays k_cache ... out are HOST arrays of n_layers device pointers.
+ * The pointer arrays k_cache ... out are HOST arrays of n_layers device pointers. Within a
+ * layer, out must not overlap q_src, k_cache or v_cache, and neither cache may overlap the
+ * other or the fresh rows (EC_ERR_INVALID_ARG).
  * cand_pos, cand_count: as for ec_select_recompute.
  * ws at least ec_step_workspace_size(p) bytes (16-byte aligned, no initial contents needed).
  * scale as for ec_partial_attention. With tau < 0, no scope and D = 128 every step is full

@@ -153,15 +153,19 @@ def test_select_and_scatter_reject_bad_args(capi):
     assert sc(ctypes.byref(good), p, p, p, p, 0, None, p, None, None) == INV
 
 
+GIB = 1 << 30  # fake buffers this far apart never overlap at the shapes used here
+
+
 def test_step_rejects_bad_args(capi):
     lib = capi.load()
     p = ctypes.c_void_p(FAKE)
     st = capi.EcState(*([p] * 11))
-    arr = (ctypes.c_void_p * 1)(FAKE)
+    # k_cache, v_cache, k_src, v_src, q_src, out: six distinct buffers
+    arrs = [(ctypes.c_void_p * 1)(FAKE + (i + 1) * GIB) for i in range(6)]
     good = _params(capi)
     big = 1 << 34
     f = lib.ec_step
-    args = lambda pp, n=1, ws=p, wsb=big: (ctypes.byref(pp), ctypes.byref(st), p, p, p, n, arr, arr, arr, arr, arr, arr,  # noqa: E731
+    args = lambda pp, n=1, ws=p, wsb=big: (ctypes.byref(pp), ctypes.byref(st), p, p, p, n, *arrs,  # noqa: E731
                                            0.088, ws, wsb, None)
     assert f(*args(_params(capi, V=50257))) == capi.EC_ERR_INVALID_ARG  # V*2 % 16 for the packed logits
     assert f(*args(good, n=-1)) == capi.EC_ERR_INVALID_ARG
@@ -171,6 +175,34 @@ def test_step_rejects_bad_args(capi):
     a = list(args(good))
     a[6] = null_arr
     assert f(*a) == capi.EC_ERR_INVALID_ARG
+
+
+def test_overlapping_buffers_are_rejected(capi):
+    # a buffer that is written while another is read must not share bytes with it: out against
+    # the queries and caches of the attention, the caches against each other and against the
+    # fresh rows of the scatter (8 MB queries and outputs, 8 MB caches at these shapes)
+    lib = capi.load()
+    INV = capi.EC_ERR_INVALID_ARG
+    good = _params(capi)
+    big = 1 << 34
+    buf = [ctypes.c_void_p(FAKE + (i + 1) * GIB) for i in range(6)]
+    ws = ctypes.c_void_p(FAKE)
+    inside = lambda b: ctypes.c_void_p(b.value + (4 << 20))  # noqa: E731  (4 MB into a buffer)
+    q, k, v, out = buf[0], buf[1], buf[2], buf[3]
+    for o in (q, k, v, inside(q), inside(k)):
+        assert lib.ec_partial_attention(ctypes.byref(good), q, k, v, ws, 0.088, o, ws, big, None, None) == INV
+        assert lib.ec_dense_attention(ctypes.byref(good), q, k, v, 0.088, o, None, None) == INV
+    # the scatter: caches against each other and against the fresh rows
+    kc, vc, kn, vn = buf[0], buf[1], buf[2], buf[3]
+    for args in [(kc, kc, kn, vn), (kc, inside(kc), kn, vn), (kc, vc, kc, vn), (kc, vc, kn, inside(vc))]:
+        assert lib.ec_kv_scatter(ctypes.byref(good), *args, 1, ws, ws, None, None) == INV
+    # the step checks every layer
+    st = capi.EcState(*([ws] * 11))
+    arrs = [(ctypes.c_void_p * 1)(b.value) for b in buf]  # k_cache, v_cache, k_src, v_src, q_src, out
+    for i, j in [(5, 4), (5, 0), (2, 0), (1, 0)]:  # out = q_src, out = k_cache, k_src = k_cache, v_cache = k_cache
+        a = list(arrs)
+        a[i] = arrs[j]
+        assert lib.ec_step(ctypes.byref(good), ctypes.byref(st), ws, ws, ws, 1, *a, 0.088, ws, big, None) == INV
 
 
 def test_read_device_error_rejects_null(capi):

@@ -301,3 +301,27 @@ def test_read_floor_validation(capi):
     assert lib.ec_read_floor(buf, 1024, None, None) == INV
     assert lib.ec_read_floor(ctypes.c_void_p((1 << 20) + 8), 1024, buf, None) == INV  # misaligned
     assert lib.ec_read_floor(buf, 1000, buf, None) == INV  # not a multiple of 16 bytes
+
+
+def test_missing_library_fails_loudly(capi, tmp_path):
+    # no fallback: loading a library that is not there raises
+    with pytest.raises(ImportError, match="no CPU fallback"):
+        capi.load(tmp_path / "libentropycache.so")
+
+
+def test_product_path_never_touches_the_oracle():
+    # the package and the input generators import nothing from oracle/, and the oracle nothing
+    # from the package (checked on the sources and in a fresh interpreter)
+    import subprocess
+    import sys
+
+    pat = re.compile(r"^\s*(import\s+oracle\b|from\s+oracle\b)", re.M)
+    for d in ("entropy_gated_kv_gb300", "workloads"):
+        for f in (ROOT / d).rglob("*.py"):
+            assert not pat.search(f.read_text()), f"{f} imports the oracle"
+    pkg = re.compile(r"^\s*(import|from)\s+entropy_gated_kv_gb300\b", re.M)
+    for f in (ROOT / "oracle").rglob("*.py"):
+        assert not pkg.search(f.read_text()), f"{f} imports the CUDA package"
+    code = "import sys, entropy_gated_kv_gb300, workloads; sys.exit(1 if 'oracle' in sys.modules else 0)"
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
